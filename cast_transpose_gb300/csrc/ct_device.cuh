@@ -1,0 +1,148 @@
+// ct_device.cuh -- small device helpers: FP8 conversion, mbarrier and TMA
+// wrappers written as inline PTX for sm_103a.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ct {
+namespace dev {
+
+// ---- FP8 conversion --------------------------------------------------------
+// Two fp32 values to two FP8 codes with round-to-nearest-even and saturation
+// to the largest finite value (the .satfinite form of the PTX cvt).  The
+// result packs `lo` in bits 0-7 and `hi` in bits 8-15.
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt_fp8x2(float lo, float hi) {
+    uint16_t r;
+    if constexpr (FMT == 0) {
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    } else {
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    }
+    return r;
+}
+
+// bf16 pair packed in a 32-bit word -> its two fp32 values (exact).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Cast 8 bf16 (one 16-byte vector) to 8 FP8 codes (two 32-bit words, byte i
+// = element i).
+template <int FMT>
+__device__ __forceinline__ uint2 cast8(const uint4& v, float scale) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t h[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float a = __fmul_rn(bf16_lo(w[e]), scale);
+        const float b = __fmul_rn(bf16_hi(w[e]), scale);
+        h[e] = cvt_fp8x2<FMT>(a, b);
+    }
+    return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+}
+
+// ---- shared-memory addresses, timers ----------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---- mbarrier ----------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete, giving up after
+// about two seconds (returns false then).  A correct launch never gets
+// near the limit; the bound only keeps a broken one from hanging the GPU.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// ---- TMA ---------------------------------------------------------------------
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 2-D tiled bulk tensor load into shared memory; completion is signalled on
+// `bar` as transaction bytes.  x is the innermost (column) coordinate.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int32_t x,
+                                            int32_t y, uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// ---- 4x4 byte transpose ------------------------------------------------------
+// r0..r3 hold rows 0..3 of a 4x4 byte block (byte k = column k); on return
+// c0..c3 hold its columns (byte i = row i).
+__device__ __forceinline__ void transpose4x4(uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3,
+                                             uint32_t& c0, uint32_t& c1, uint32_t& c2,
+                                             uint32_t& c3) {
+    const uint32_t t0 = __byte_perm(r0, r1, 0x5140);  // r0.b0 r1.b0 r0.b1 r1.b1
+    const uint32_t t1 = __byte_perm(r2, r3, 0x5140);  // r2.b0 r3.b0 r2.b1 r3.b1
+    const uint32_t t2 = __byte_perm(r0, r1, 0x7362);  // r0.b2 r1.b2 r0.b3 r1.b3
+    const uint32_t t3 = __byte_perm(r2, r3, 0x7362);  // r2.b2 r3.b2 r2.b3 r3.b3
+    c0 = __byte_perm(t0, t1, 0x5410);
+    c1 = __byte_perm(t0, t1, 0x7632);
+    c2 = __byte_perm(t2, t3, 0x5410);
+    c3 = __byte_perm(t2, t3, 0x7632);
+}
+
+// Max of the two bf16 magnitudes (sign cleared) of a packed pair, kept as a
+// pair so that one SIMD max per word suffices.
+__device__ __forceinline__ uint32_t absmax_pair(uint32_t acc, uint32_t w) {
+    return __vmaxu2(acc, w & 0x7FFF7FFFu);
+}
+
+// Collapse a pair accumulator into the fp32 bit pattern of the larger
+// magnitude (bf16 widened to fp32).
+__device__ __forceinline__ uint32_t pair_to_f32_bits(uint32_t acc) {
+    const uint32_t a = acc & 0xFFFFu, b = acc >> 16;
+    return (a > b ? a : b) << 16;
+}
+
+}  // namespace dev
+}  // namespace ct

@@ -1,0 +1,273 @@
+// ct_general.cu -- kernels for the cases the TMA path does not take, and the
+// small kernels around it (sm_103a):
+//   * general_cast_kernel: cast (+ transpose, + dbias partials) of a bf16
+//     matrix of ANY shape and alignment, 128x32 tiles, element-wise loads;
+//   * dbias_finish_kernel: db[j] = sum over 128-row tiles of the partials,
+//     in fp64, in a fixed order (deterministic);
+//   * scale_update_kernel: the delayed-scaling update of "[PyTorch] Refactor
+//     FP8 workspaces in linear modules" (Motivations: scale update kernel,
+//     infinite-scale case), one thread per tensor;
+//   * transpose kernels for FP8 bytes (the lazy transpose-cache fill of the
+//     same page), a 128x128-tile vectorised one and a general one.
+#include "ct_device.cuh"
+#include "ct_internal.h"
+
+#include <cmath>
+
+namespace ct {
+namespace {
+
+// ---------------------------------------------------------------------------
+// General cast: tile = 128 rows x 32 columns, 256 threads; thread (c, g)
+// handles column c and rows g + 8*i, i = 0..15.
+constexpr int kGenCols = 32;
+
+template <int FMT, bool DBIAS>
+__global__ void __launch_bounds__(256) general_cast_kernel(GeneralArgs a) {
+    if (a.noop != nullptr && *a.noop != 0.0f) return;
+    __shared__ uint8_t tileq[kTileRows][kGenCols + 4];
+    __shared__ float colsum[8][kGenCols];
+    __shared__ unsigned s_amax;
+
+    const int64_t tiles_c = (a.cols + kGenCols - 1) / kGenCols;
+    const int64_t tiles = ((a.rows + kTileRows - 1) / kTileRows) * tiles_c;
+    const int tid = threadIdx.x;
+    const int c = tid & 31;
+    const int g = tid >> 5;
+    const float scale = *a.scale;
+    uint32_t amax = 0;
+    if (tid == 0) s_amax = 0;
+    __syncthreads();
+
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        const int64_t rt = tile / tiles_c;
+        const int64_t row0 = rt * kTileRows;
+        const int64_t col0 = (tile - rt * tiles_c) * kGenCols;
+        const int64_t col = col0 + c;
+        float cs = 0.0f;
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+            const int r = g + 8 * i;
+            const int64_t row = row0 + r;
+            uint8_t code = 0;
+            if (row < a.rows && col < a.cols) {
+                const uint32_t bits = a.x[row * a.cols + col];
+                const uint32_t mag = (bits & 0x7FFFu) << 16;
+                amax = mag > amax ? mag : amax;
+                const float f = __uint_as_float(bits << 16);
+                if (DBIAS) cs += f;
+                code = static_cast<uint8_t>(dev::cvt_fp8x2<FMT>(__fmul_rn(f, scale), 0.0f));
+                if (a.out) a.out[row * a.cols + col] = code;
+            }
+            tileq[r][c] = code;
+        }
+        if (DBIAS) colsum[g][c] = cs;
+        __syncthreads();
+        if (a.out_t) {
+            // lanes run along rows of x, i.e. along a row of the transpose
+            const int r = tid & (kTileRows - 1);
+            const int64_t row = row0 + r;
+            for (int cc = tid >> 7; cc < kGenCols; cc += 2) {
+                const int64_t tc = col0 + cc;
+                if (row < a.rows && tc < a.cols) a.out_t[tc * a.rows + row] = tileq[r][cc];
+            }
+        }
+        if (DBIAS && tid < kGenCols && col < a.cols) {
+            float s = colsum[0][tid];
+            for (int j = 1; j < 8; ++j) s += colsum[j][tid];
+            a.partial[rt * a.cols + col] = s;
+        }
+        if (tile == 0 && tid == 0) *a.scale_inv = __fdiv_rn(1.0f, scale);
+        __syncthreads();
+    }
+    const unsigned m = __reduce_max_sync(0xFFFFFFFFu, amax);
+    if ((tid & 31) == 0 && m != 0) atomicMax(&s_amax, m);
+    __syncthreads();
+    if (tid == 0 && s_amax != 0) atomicMax(reinterpret_cast<unsigned*>(a.amax), s_amax);
+}
+
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) dbias_finish_kernel(const float* __restrict__ partial,
+                                                           int64_t row_tiles, int64_t cols,
+                                                           float* __restrict__ db,
+                                                           const float* noop) {
+    if (noop != nullptr && *noop != 0.0f) return;
+    for (int64_t j = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; j < cols;
+         j += int64_t(gridDim.x) * blockDim.x) {
+        double s = 0.0;
+        for (int64_t t = 0; t < row_tiles; ++t) s += static_cast<double>(partial[t * cols + j]);
+        db[j] = static_cast<float>(s);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Delayed scaling, one thread per tensor i:
+//   a = max over the L history rows (NaN propagates, the first NaN is kept),
+//   s = (fp8_max / a) / 2^margin, kept only when a > 0, a finite, s finite,
+//   scale_inv = 1 / scale, then the window slides by one row.
+__global__ void __launch_bounds__(128) scale_update_kernel(float* __restrict__ hist,
+                                                           float* __restrict__ scale,
+                                                           float* __restrict__ scale_inv,
+                                                           int L, int n, float fp8_max,
+                                                           float two_pow_margin,
+                                                           const float* noop) {
+    if (noop != nullptr && *noop != 0.0f) return;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    float a = hist[i];
+    for (int r = 1; r < L; ++r) {
+        if (isnan(a)) break;
+        const float v = hist[int64_t(r) * n + i];
+        if (isnan(v) || v > a) a = v;
+    }
+    float s = scale[i];
+    if (a > 0.0f && isfinite(a)) {
+        const float cand = __fdiv_rn(__fdiv_rn(fp8_max, a), two_pow_margin);
+        if (isfinite(cand)) s = cand;
+    }
+    scale[i] = s;
+    scale_inv[i] = __fdiv_rn(1.0f, s);
+    for (int r = L - 1; r >= 1; --r) hist[int64_t(r) * n + i] = hist[int64_t(r - 1) * n + i];
+    hist[i] = 0.0f;
+}
+
+// ---------------------------------------------------------------------------
+// FP8 transpose, 128x128 byte tiles, 256 threads.  Loads are 16-byte row
+// vectors; the tile is kept in shared memory with the same XOR swizzle as
+// the cast kernel's FP8 copy (word w of row r at w ^ 4*(r/16)), so both the
+// row-vector stores and the 16x4 column gathers are conflict-free.
+__global__ void __launch_bounds__(256) transpose_fast_kernel(const uint8_t* __restrict__ in,
+                                                             int64_t rows, int64_t cols,
+                                                             uint8_t* __restrict__ out,
+                                                             const float* noop) {
+    if (noop != nullptr && *noop != 0.0f) return;
+    __shared__ __align__(16) uint32_t tile[kTileRows * (kTileCols / 4)];
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int64_t tiles_c = (cols + kTileCols - 1) / kTileCols;
+    const int64_t tiles = ((rows + kTileRows - 1) / kTileRows) * tiles_c;
+    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+        const int64_t rt = t / tiles_c;
+        const int64_t row0 = rt * kTileRows, col0 = (t - rt * tiles_c) * kTileCols;
+        // load: chunk ch (16 bytes = 4 words) of row r; 1024 chunks, 4 per thread
+        uint4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int idx = tid + 256 * i;
+            const int r = idx >> 3, ch = idx & 7;
+            const int64_t row = row0 + r, col = col0 + 16 * ch;
+            v[i] = (row < rows && col < cols)
+                       ? __ldg(reinterpret_cast<const uint4*>(in + row * cols + col))
+                       : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int idx = tid + 256 * i;
+            const int r = idx >> 3, ch = idx & 7;
+            *reinterpret_cast<uint4*>(&tile[r * 32 + ((4 * ch) ^ (4 * (r >> 4)))]) = v[i];
+        }
+        __syncthreads();
+        const int b = lane & 7, w = warp * 4 + (lane >> 3);
+        uint32_t rw[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) rw[j] = tile[(16 * b + j) * 32 + (w ^ (4 * b))];
+        uint32_t o[4][4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+            dev::transpose4x4(rw[4 * g], rw[4 * g + 1], rw[4 * g + 2], rw[4 * g + 3], o[0][g],
+                              o[1][g], o[2][g], o[3][g]);
+        const int64_t row = row0 + 16 * b;
+        if (row < rows) {
+#pragma unroll
+            for (int kq = 0; kq < 4; ++kq) {
+                const int64_t col = col0 + 4 * w + kq;
+                if (col < cols)
+                    *reinterpret_cast<uint4*>(out + col * rows + row) =
+                        make_uint4(o[kq][0], o[kq][1], o[kq][2], o[kq][3]);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// General byte transpose: 32x32 tiles, any shape and alignment.
+__global__ void __launch_bounds__(256) transpose_general_kernel(const uint8_t* __restrict__ in,
+                                                                int64_t rows, int64_t cols,
+                                                                uint8_t* __restrict__ out,
+                                                                const float* noop) {
+    if (noop != nullptr && *noop != 0.0f) return;
+    __shared__ uint8_t tile[32][33];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int64_t tiles_c = (cols + 31) / 32;
+    const int64_t tiles = ((rows + 31) / 32) * tiles_c;
+    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+        const int64_t rt = t / tiles_c;
+        const int64_t row0 = rt * 32, col0 = (t - rt * tiles_c) * 32;
+        for (int r = ty; r < 32; r += 8) {
+            const int64_t row = row0 + r, col = col0 + tx;
+            if (row < rows && col < cols) tile[r][tx] = in[row * cols + col];
+        }
+        __syncthreads();
+        for (int cc = ty; cc < 32; cc += 8) {
+            const int64_t col = col0 + cc, row = row0 + tx;
+            if (row < rows && col < cols) out[col * rows + row] = tile[tx][cc];
+        }
+        __syncthreads();
+    }
+}
+
+unsigned grid_for(int64_t tiles, int64_t cap) {
+    if (tiles < 1) tiles = 1;
+    return static_cast<unsigned>(tiles < cap ? tiles : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_general(const GeneralArgs& a, int fmt, cudaStream_t stream) {
+    const int64_t tiles =
+        ((a.rows + kTileRows - 1) / kTileRows) * ((a.cols + kGenCols - 1) / kGenCols);
+    const unsigned grid = grid_for(tiles, 1 << 20);
+    const bool dbias = a.partial != nullptr;
+    if (fmt == 0) {
+        if (dbias) general_cast_kernel<0, true><<<grid, 256, 0, stream>>>(a);
+        else general_cast_kernel<0, false><<<grid, 256, 0, stream>>>(a);
+    } else {
+        if (dbias) general_cast_kernel<1, true><<<grid, 256, 0, stream>>>(a);
+        else general_cast_kernel<1, false><<<grid, 256, 0, stream>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dbias_finish(const float* partial, int64_t row_tiles, int64_t cols,
+                                float* dbias, const float* noop, cudaStream_t stream) {
+    const unsigned grid = grid_for((cols + 255) / 256, 1 << 16);
+    dbias_finish_kernel<<<grid, 256, 0, stream>>>(partial, row_tiles, cols, dbias, noop);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scale_update(float* hist, float* scale, float* scale_inv, int hist_len,
+                                int n, int fmt, int margin, const float* noop,
+                                cudaStream_t stream) {
+    const float fp8_max = fmt == 0 ? 448.0f : 57344.0f;
+    const float two_pow_margin = std::ldexp(1.0f, margin);   // exact for 0 <= margin <= 126
+    const unsigned grid = static_cast<unsigned>((n + 127) / 128);
+    scale_update_kernel<<<grid, 128, 0, stream>>>(hist, scale, scale_inv, hist_len, n, fp8_max,
+                                                  two_pow_margin, noop);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose(const uint8_t* in, int64_t rows, int64_t cols, uint8_t* out,
+                             const float* noop, bool fast, cudaStream_t stream) {
+    if (fast) {
+        const int64_t tiles = ((rows + 127) / 128) * ((cols + 127) / 128);
+        transpose_fast_kernel<<<grid_for(tiles, 4096), 256, 0, stream>>>(in, rows, cols, out,
+                                                                          noop);
+    } else {
+        const int64_t tiles = ((rows + 31) / 32) * ((cols + 31) / 32);
+        transpose_general_kernel<<<grid_for(tiles, 1 << 20), 256, 0, stream>>>(in, rows, cols,
+                                                                                out, noop);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace ct

@@ -1,0 +1,94 @@
+// ct_internal.h -- shared declarations between the host ABI layer and the
+// CUDA translation units of the cast-transpose library.  Not installed.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ct {
+
+// Tile of the TMA-staged kernels: 128 rows x 128 columns of bf16 (32 KB),
+// processed by 256 threads.  Dbias partial sums are kept per 128-row tile by
+// every kernel, so the workspace layout is [ceil(rows/128), cols] fp32.
+constexpr int kTileRows = 128;
+constexpr int kTileCols = 128;
+constexpr int kThreads = 256;
+constexpr int kMaxListPerLaunch = 64;
+
+// Bit set in the device diagnostic word when an mbarrier wait gave up.
+constexpr unsigned kErrWaitTimeout = 1u;
+
+// One tensor of a TMA-path launch.  Pointers are device pointers.
+struct FastTensor {
+    uint8_t* out;          // [rows, cols] FP8 codes (may be null: not written)
+    uint8_t* out_t;        // [cols, rows] FP8 codes (null when no transpose)
+    const float* scale;
+    float* amax;
+    float* scale_inv;
+    int64_t rows;
+    int64_t cols;
+    int64_t tile_begin;    // first global tile index of this tensor
+    int64_t tile_end;      // one past its last global tile index
+    int64_t tile_cols;     // tiles per row of tiles
+};
+
+template <int NT>
+struct FastParams {
+    CUtensorMap map[NT];   // TMA descriptors of the bf16 inputs (64-B aligned)
+    FastTensor t[NT];
+    int n;
+    int64_t total_tiles;
+    const float* noop;     // nullable device flag
+    float* partial;        // dbias partials [ceil(rows/128), cols], or null
+};
+
+// Arguments of the general (any shape / alignment) kernels.
+struct GeneralArgs {
+    const uint16_t* x;
+    uint8_t* out;          // may be null
+    uint8_t* out_t;        // may be null
+    const float* scale;
+    float* amax;
+    float* scale_inv;
+    float* partial;        // dbias partials or null
+    int64_t rows;
+    int64_t cols;
+    const float* noop;
+};
+
+enum class Fmt : int { E4M3 = 0, E5M2 = 1 };
+
+// ---- launchers (return cudaGetLastError() of the launch) -----------------
+// TMA path.  `variant`: 0 = cast + transpose, 1 = cast only.  `dbias`
+// requires n == 1 and variant 0.
+cudaError_t launch_fast(const FastParams<1>& p, int fmt, bool dbias, int variant,
+                        cudaStream_t stream);
+cudaError_t launch_fast_list(const FastParams<kMaxListPerLaunch>& p, int fmt,
+                             cudaStream_t stream);
+
+// General path.
+cudaError_t launch_general(const GeneralArgs& a, int fmt, cudaStream_t stream);
+
+// Dbias finish: db[j] = sum over row tiles of partial[rt, j] (fp64 sum).
+cudaError_t launch_dbias_finish(const float* partial, int64_t row_tiles, int64_t cols,
+                                float* dbias, const float* noop, cudaStream_t stream);
+
+// Scale update.
+cudaError_t launch_scale_update(float* hist, float* scale, float* scale_inv, int hist_len,
+                                int n, int fmt, int margin, const float* noop,
+                                cudaStream_t stream);
+
+// FP8 byte transpose.  `fast` requires rows % 16 == 0, cols % 16 == 0 and
+// 16-byte aligned pointers.
+cudaError_t launch_transpose(const uint8_t* in, int64_t rows, int64_t cols, uint8_t* out,
+                             const float* noop, bool fast, cudaStream_t stream);
+
+// Diagnostic word (device of the calling thread).
+cudaError_t read_device_error(unsigned* value, bool clear);
+
+// Number of SMs and persistent CTAs per SM for the TMA kernels of this
+// device (cached per device).
+int persistent_grid(int variant_key, int device);
+
+}  // namespace ct

@@ -1,0 +1,228 @@
+/*
+ * cast_transpose.h -- C ABI of the GB300 (sm_103a) FP8 cast-transpose library.
+ *
+ * The library turns bf16 matrices into FP8 tensors for delayed-scaling
+ * training: the FP8 bytes, their transpose, the amax that feeds the next
+ * scale, and the tensor's own scale-inverse, all in one pass over HBM.
+ *
+ * Sources of the operations (pages of the NVIDIA TransformerEngine project):
+ *   [A] "[PyTorch] cuda graph support": the DbiasCastTranspose example in the
+ *       transpose-cache discussion (db = dy.sum(dim=0); dx = cast_transpose(dy),
+ *       an FP8 tensor with its transpose cached); the feature list (amaxes
+ *       reduced within the current iteration; transposes made persistent for
+ *       graph capture; scale-inverses no longer frozen).
+ *   [B] "[PyTorch] Refactor FP8 workspaces in linear modules": Motivations
+ *       (the FP8 tensor keeps a private scale-inverse that matches its bytes;
+ *       the scale update kernel; the too-tiny-amax / infinite-scale case;
+ *       the cost of a separate scale-inverse initialisation launch) and the
+ *       lazy transpose-caching bullet (the transpose kernel must still be
+ *       captured in a CUDA graph and skipped at replay through a noop flag).
+ *   [C] "[PyTorch] Userbuffers support in operation-based API": FP8 tensors
+ *       are built on caller-provided data / data_transpose buffers.
+ *
+ * FP8 formats: E4M3 (bias 7, largest normal 448, no infinities) and E5M2
+ * (bias 15, largest normal 57344), as in the OCP OFP8 specification.  The
+ * cast computes q = fp8(fp32(x) * scale): one IEEE fp32 multiply, then
+ * round-to-nearest-even with saturation (values beyond the largest normal
+ * and +-Inf become +-max; NaN becomes the canonical NaN 0x7F).  No
+ * flush-to-zero.
+ *
+ * Conventions that hold for every entry point:
+ *   - Every pointer is a DEVICE pointer owned by the caller, unless the
+ *     argument says "host".  Matrices are dense and row-major; "rows x cols"
+ *     data has element (i, j) at offset i*cols + j; the transpose of a
+ *     rows x cols matrix is a cols x rows matrix.
+ *   - The library allocates no device memory, never synchronises the stream
+ *     or the device, and never reads device memory from the host, so every
+ *     call can be recorded in a CUDA graph.  `stream` is a cudaStream_t
+ *     (NULL = the legacy default stream).
+ *   - `noop_flag` (nullable) is a device fp32 scalar read by the kernels at
+ *     run time: when it is nonzero the call writes nothing at all (no data,
+ *     transpose, amax, scale-inverse, dbias, history or scale).  This is how
+ *     a captured graph skips a cached transpose [B].
+ *   - `amax` is max-merged: the kernel stores max(*amax, max|x|), comparing
+ *     IEEE magnitude bit patterns (NaN above Inf, so a NaN in x propagates).
+ *     *amax must hold a non-negative value (normally 0, the cleared current
+ *     slot of the amax history) before the call.
+ *   - Arguments are checked on the host before anything is launched; a bad
+ *     argument returns an error code and launches nothing.  rows == 0 or
+ *     cols == 0 returns CT_OK without a launch and writes nothing (its
+ *     pointers are then not checked and may be NULL).  A failed launch returns
+ *     CT_ERR_CUDA.  Any shape and alignment is accepted: dense shapes whose
+ *     row lengths are multiples of 16 bytes and 16-byte-aligned buffers take
+ *     the TMA-staged fast path, everything else a slower general kernel
+ *     with identical results.
+ *   - Calls are thread-safe; the library keeps no per-call state.
+ */
+#ifndef CAST_TRANSPOSE_GB300_H
+#define CAST_TRANSPOSE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CT_E4M3 = 0,
+    CT_E5M2 = 1
+} ct_fp8_format;
+
+typedef enum {
+    CT_OK = 0,
+    CT_ERR_NULL = 1,        /* a required pointer is NULL                      */
+    CT_ERR_SHAPE = 2,       /* negative size, or a size the kernels cannot index */
+    CT_ERR_ALIGN = 3,       /* buffer misaligned for its element type          */
+    CT_ERR_FORMAT = 4,      /* fmt is not CT_E4M3 / CT_E5M2                    */
+    CT_ERR_ARG = 5,         /* other invalid scalar (history length, margin)   */
+    CT_ERR_ALIAS = 6,       /* an output overlaps an input or another output   */
+    CT_ERR_WORKSPACE = 7,   /* workspace missing or too small                  */
+    CT_ERR_CUDA = 8         /* a CUDA runtime call or launch failed            */
+} ct_status;
+
+/* Human-readable name of a ct_status value (static string, never NULL). */
+const char* ct_status_string(int status);
+
+/*
+ * fp8_cast_transpose -- [A] cast_transpose(dy), [B] private scale-inverse.
+ *
+ *   x          bf16 [rows, cols] input (read only)
+ *   scale      fp32 scalar: the scale to cast with
+ *   amax       fp32 scalar, max-merged with max|x| (see conventions)
+ *   scale_inv  fp32 scalar output: 1 / *scale (IEEE division), the FP8
+ *              tensor's own scale-inverse; must not alias `scale`
+ *   out        uint8 [rows, cols] output: FP8 codes of x * scale
+ *   out_t      uint8 [cols, rows] output: the transpose of `out`
+ *   fmt        CT_E4M3 or CT_E5M2
+ *   noop_flag  nullable fp32 device scalar; nonzero -> nothing is written
+ *
+ * Outputs must not overlap the input or each other.  Errors: CT_ERR_NULL,
+ * CT_ERR_SHAPE, CT_ERR_ALIGN (x not 2-byte aligned), CT_ERR_FORMAT,
+ * CT_ERR_ALIAS, CT_ERR_CUDA.
+ */
+int fp8_cast_transpose(const void* x, int64_t rows, int64_t cols,
+                       const float* scale, float* amax, float* scale_inv,
+                       void* out, void* out_t, int fmt,
+                       const float* noop_flag, void* stream);
+
+/*
+ * fp8_dbias_cast_transpose -- [A] DbiasCastTranspose.backward:
+ * db = dy.sum(dim=0) next to cast_transpose(dy), in one pass over dy.
+ *
+ *   dy, scale, amax, scale_inv, out, out_t, fmt, noop_flag: as in
+ *              fp8_cast_transpose, with dy in place of x
+ *   dbias      fp32 [cols] output: column sums of the unscaled dy,
+ *              accumulated in fp32 per 128-row tile and in fp64 across tiles;
+ *              deterministic (the summation order depends only on the shape)
+ *   workspace  device scratch of at least
+ *              fp8_dbias_cast_transpose_workspace_size(rows, cols) bytes,
+ *              16-byte aligned; its contents on entry are ignored and on exit
+ *              undefined; calls that overlap in time need separate workspaces
+ *
+ * Two kernels are launched on `stream` (the fused pass, then a small
+ * column-sum finish).  Errors: as fp8_cast_transpose, plus CT_ERR_WORKSPACE.
+ */
+int fp8_dbias_cast_transpose(const void* dy, int64_t rows, int64_t cols,
+                             const float* scale, float* amax, float* scale_inv,
+                             void* out, void* out_t, float* dbias,
+                             void* workspace, size_t workspace_bytes, int fmt,
+                             const float* noop_flag, void* stream);
+
+/* Bytes of workspace fp8_dbias_cast_transpose needs for a rows x cols dy
+ * (0 when rows or cols is 0 or negative). */
+size_t fp8_dbias_cast_transpose_workspace_size(int64_t rows, int64_t cols);
+
+/* One entry of a tensor list (host memory; the pointers inside are device
+ * pointers with the meaning they have in fp8_cast_transpose). */
+typedef struct {
+    const void* x;
+    int64_t rows;
+    int64_t cols;
+    const float* scale;
+    float* amax;
+    float* scale_inv;
+    void* out;
+    void* out_t;
+} ct_tensor_desc;
+
+/*
+ * fp8_multi_cast_transpose -- cast-transpose of a list of tensors, each with
+ * its own scale, amax and scale-inverse, in one persistent launch ([B]: many
+ * FP8 weight workspaces are refreshed every step; one launch instead of one
+ * per tensor keeps the host overhead flat).
+ *
+ *   descs      HOST array of n descriptors, read during the call only
+ *   n          number of descriptors (>= 0); lists longer than 64 tensors,
+ *              and tensors that miss the fast path's shape/alignment rules,
+ *              are split across further launches on the same stream
+ *   fmt        one FP8 format for the whole list
+ *   noop_flag  as above, for the whole list
+ *
+ * Every descriptor is validated before anything is launched.  Entries with
+ * rows == 0 or cols == 0 are skipped.  Distinct entries must not share
+ * outputs.  Errors: as fp8_cast_transpose (the first bad entry decides).
+ */
+int fp8_multi_cast_transpose(const ct_tensor_desc* descs, int n, int fmt,
+                             const float* noop_flag, void* stream);
+
+/*
+ * fp8_amax_and_scale_update -- the delayed-scaling scale update kernel [B]
+ * for n tensors, including the infinite-scale guard.
+ *
+ *   amax_history  fp32 [hist_len, n] row-major; row 0 holds the amaxes of the
+ *                 step that just ran (written by the cast kernels)
+ *   scale         fp32 [n], read and written
+ *   scale_inv     fp32 [n], written: 1 / scale (the recipe's copy; tensors
+ *                 cast earlier keep their own copy, [B])
+ *   hist_len      L >= 1;  n >= 0;  margin in [0, 126];  fmt as above
+ *
+ * For each tensor i:
+ *   a = max over the L history rows of column i (NaN propagates);
+ *   s = (fp8_max / a) / 2^margin in fp32 (fp8_max = 448 or 57344);
+ *   scale[i] = s unless a is not > 0, a is not finite, or s is not finite
+ *   (the too-tiny-amax case), in which case scale[i] is left as it was;
+ *   scale_inv[i] = 1 / scale[i];
+ *   then the window slides: row r takes row r-1 for r = L-1 .. 1, and row 0
+ *   is set to 0, ready for the next step's max-merge.
+ * One launch.  Buffers must not overlap.  Errors: CT_ERR_NULL, CT_ERR_ARG,
+ * CT_ERR_FORMAT, CT_ERR_ALIGN, CT_ERR_ALIAS, CT_ERR_CUDA.
+ */
+int fp8_amax_and_scale_update(float* amax_history, float* scale, float* scale_inv,
+                              int hist_len, int n, int fmt, int margin,
+                              const float* noop_flag, void* stream);
+
+/*
+ * fp8_transpose -- byte transpose of an existing FP8 tensor: the lazy
+ * transpose-cache fill of [B] (transpose_2d(cache=True)), skippable through
+ * the noop flag inside a captured graph.
+ *
+ *   in         uint8 [rows, cols]
+ *   out        uint8 [cols, rows], must not overlap `in`
+ */
+int fp8_transpose(const void* in, int64_t rows, int64_t cols, void* out,
+                  const float* noop_flag, void* stream);
+
+/*
+ * fp8_cast -- the cast without the transpose (Float8Tensor.to_float8 in the
+ * FP8Linear example of [A]): out, amax and scale_inv as in
+ * fp8_cast_transpose, no transposed output.
+ */
+int fp8_cast(const void* x, int64_t rows, int64_t cols, const float* scale,
+             float* amax, float* scale_inv, void* out, int fmt,
+             const float* noop_flag, void* stream);
+
+/*
+ * ct_device_error -- diagnostic word of the current device.  Kernels that
+ * wait on an mbarrier give up after a bounded time (about two seconds)
+ * instead of hanging, set a bit here and return early; in a correct run it
+ * stays 0.  Reads (synchronously) and optionally clears the word.
+ * Bits: 1 = a tile-load wait timed out.
+ */
+int ct_device_error(unsigned int* value_out, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CAST_TRANSPOSE_GB300_H */

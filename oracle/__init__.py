@@ -64,6 +64,7 @@ def lib() -> ctypes.CDLL:
             L.oracle_cast_transpose.argtypes = [c.c_void_p, c.c_int64, c.c_int64, c.c_float,
                                                 c.c_int, c.c_void_p, c.c_void_p, c.c_void_p,
                                                 c.c_void_p]
+            L.oracle_amax.argtypes = [c.c_void_p, c.c_int64, c.c_void_p]
             L.oracle_dbias.argtypes = [c.c_void_p, c.c_int64, c.c_int64, c.c_void_p]
             L.oracle_fp8_transpose.argtypes = [c.c_void_p, c.c_int64, c.c_int64, c.c_void_p]
             L.oracle_amax_and_scale_update.argtypes = [c.c_void_p, c.c_void_p, c.c_void_p,
@@ -119,6 +120,14 @@ def cast_transpose(x, scale: float, fmt: int, amax_in: float = 0.0,
                                 _ptr(qt) if qt is not None else None,
                                 _ptr(amax), _ptr(sinv))
     return {"q": q, "qt": qt, "amax": amax[0], "scale_inv": sinv[0]}
+
+
+def amax(x, amax_in: float = 0.0) -> np.float32:
+    """max(amax_in, max |x|) by IEEE magnitude bit pattern (NaN propagates)."""
+    x = _bits16(x)
+    out = np.array([amax_in], dtype=np.float32)
+    lib().oracle_amax(_ptr(x), x.size, _ptr(out))
+    return out[0]
 
 
 def dbias(x) -> np.ndarray:

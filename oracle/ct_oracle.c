@@ -167,6 +167,12 @@ static void merge_amax(const uint16_t* x, int64_t count, float* amax_io)
     *amax_io = f32_from_bits(best);
 }
 
+/* amax alone: max-merge of max |x| into *amax_io (as in the cast below). */
+void oracle_amax(const uint16_t* x, int64_t count, float* amax_io)
+{
+    merge_amax(x, count, amax_io);
+}
+
 /* Cast + transpose + amax + scale-inverse of one row-major bf16 matrix.
  *   q[i*cols + j]  = encode(bf16(x[i,j]) * scale)
  *   qt[j*rows + i] = q[i*cols + j]

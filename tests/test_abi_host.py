@@ -1,0 +1,150 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must load without a GPU, export every function that
+include/cast_transpose.h declares, and reject bad arguments on the host
+with the documented status codes before anything is launched.  Only calls
+that are rejected (or that have nothing to do) are made here: the pointers
+passed are never dereferenced.
+"""
+import ctypes
+
+import pytest
+
+import cast_transpose_gb300 as ct
+
+CT_OK, CT_ERR_NULL, CT_ERR_SHAPE, CT_ERR_ALIGN, CT_ERR_FORMAT, CT_ERR_ARG, CT_ERR_ALIAS, \
+    CT_ERR_WORKSPACE, CT_ERR_CUDA = range(9)
+
+# fake, well-separated, 256-byte aligned "device" addresses: never dereferenced
+X, Q, QT, S, A, SI, DB, WS, NOOP = (0x10000000 * (i + 1) for i in range(9))
+
+
+@pytest.fixture(scope="module")
+def L():
+    return ct.lib()
+
+
+def test_exports_every_declared_function(L):
+    names = ct.header_functions()
+    expected = {"fp8_cast_transpose", "fp8_dbias_cast_transpose",
+                "fp8_dbias_cast_transpose_workspace_size", "fp8_multi_cast_transpose",
+                "fp8_amax_and_scale_update", "fp8_transpose", "fp8_cast", "ct_status_string",
+                "ct_device_error"}
+    assert expected <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    for s in range(9):
+        assert L.ct_status_string(s).decode().startswith("CT_")
+    assert L.ct_status_string(99) == b"unknown status"
+
+
+def _ct(L, x=X, rows=64, cols=64, scale=S, amax=A, sinv=SI, q=Q, qt=QT, fmt=0):
+    return L.fp8_cast_transpose(x, rows, cols, scale, amax, sinv, q, qt, fmt, None, None)
+
+
+def test_cast_transpose_rejects(L):
+    assert _ct(L, x=None) == CT_ERR_NULL
+    assert _ct(L, q=None) == CT_ERR_NULL
+    assert _ct(L, qt=None) == CT_ERR_NULL
+    assert _ct(L, scale=None) == CT_ERR_NULL
+    assert _ct(L, fmt=2) == CT_ERR_FORMAT
+    assert _ct(L, fmt=-1) == CT_ERR_FORMAT
+    assert _ct(L, rows=-1) == CT_ERR_SHAPE
+    assert _ct(L, cols=-5) == CT_ERR_SHAPE
+    assert _ct(L, rows=1 << 40, cols=1 << 20) == CT_ERR_SHAPE
+    assert _ct(L, x=X + 1) == CT_ERR_ALIGN
+    assert _ct(L, amax=A + 2) == CT_ERR_ALIGN
+    assert _ct(L, q=X) == CT_ERR_ALIAS                 # output over the input
+    assert _ct(L, qt=Q + 100) == CT_ERR_ALIAS          # outputs overlap
+    assert _ct(L, sinv=S) == CT_ERR_ALIAS              # scale_inv over scale
+    assert _ct(L, amax=SI) == CT_ERR_ALIAS
+
+
+def test_empty_shapes_are_ok_without_launch(L):
+    assert _ct(L, rows=0) == CT_OK
+    assert _ct(L, cols=0) == CT_OK
+    assert L.fp8_cast(X, 0, 7, S, A, SI, Q, 0, None, None) == CT_OK
+    assert L.fp8_transpose(X, 5, 0, Q, None, None) == CT_OK
+
+
+def test_dbias_rejects(L):
+    need = L.fp8_dbias_cast_transpose_workspace_size(300, 70)
+    assert need == ((300 + 127) // 128) * 70 * 4 + 8   # rounded up to 16 bytes
+    assert L.fp8_dbias_cast_transpose_workspace_size(0, 70) == 0
+    assert L.fp8_dbias_cast_transpose_workspace_size(-3, 70) == 0
+
+    def call(ws=WS, nbytes=need, db=DB, rows=300, cols=70):
+        return L.fp8_dbias_cast_transpose(X, rows, cols, S, A, SI, Q, QT, db, ws, nbytes, 1,
+                                          None, None)
+    assert call(db=None) == CT_ERR_NULL
+    assert call(ws=None) == CT_ERR_WORKSPACE
+    assert call(nbytes=need - 1) == CT_ERR_WORKSPACE
+    assert call(ws=WS + 4) == CT_ERR_ALIGN
+    assert call(db=DB + 2) == CT_ERR_ALIGN
+    assert call(db=X) == CT_ERR_ALIAS
+    assert call(ws=Q) == CT_ERR_ALIAS
+    assert call(rows=0) == CT_OK
+
+
+def test_update_rejects(L):
+    def call(h=X, s=S, si=SI, L_=16, n=4, fmt=0, margin=0):
+        return L.fp8_amax_and_scale_update(h, s, si, L_, n, fmt, margin, None, None)
+    assert call(L_=0) == CT_ERR_ARG
+    assert call(n=-1) == CT_ERR_ARG
+    assert call(margin=-1) == CT_ERR_ARG
+    assert call(margin=127) == CT_ERR_ARG
+    assert call(fmt=3) == CT_ERR_FORMAT
+    assert call(h=None) == CT_ERR_NULL
+    assert call(s=S + 1) == CT_ERR_ALIGN
+    assert call(si=S) == CT_ERR_ALIAS
+    assert call(s=X + 8) == CT_ERR_ALIAS               # scale inside the history
+    assert call(n=0) == CT_OK
+
+
+def test_transpose_and_cast_reject(L):
+    assert L.fp8_transpose(None, 4, 4, Q, None, None) == CT_ERR_NULL
+    assert L.fp8_transpose(X, -4, 4, Q, None, None) == CT_ERR_SHAPE
+    assert L.fp8_transpose(X, 4, 4, X + 8, None, None) == CT_ERR_ALIAS
+    assert L.fp8_cast(X, 4, 4, S, A, SI, None, 0, None, None) == CT_ERR_NULL
+    assert L.fp8_cast(X, 4, 4, S, A, SI, X, 0, None, None) == CT_ERR_ALIAS
+
+
+def _desc(x=X, rows=64, cols=64, scale=S, amax=A, sinv=SI, q=Q, qt=QT):
+    return ct._Desc(x, rows, cols, scale, amax, sinv, q, qt)
+
+
+def test_multi_rejects(L):
+    arr = (ct._Desc * 2)
+    assert L.fp8_multi_cast_transpose(None, 0, 0, None, None) == CT_OK
+    assert L.fp8_multi_cast_transpose(None, 2, 0, None, None) == CT_ERR_NULL
+    assert L.fp8_multi_cast_transpose(arr(), -1, 0, None, None) == CT_ERR_ARG
+    good = _desc()
+    other = _desc(x=X + 0x100000, q=Q + 0x100000, qt=QT + 0x100000, amax=A + 64, sinv=SI + 64,
+                  scale=S + 64)
+    assert L.fp8_multi_cast_transpose(arr(good, _desc(qt=None)), 2, 0, None, None) == CT_ERR_NULL
+    assert L.fp8_multi_cast_transpose(arr(good, other), 2, 9, None, None) == CT_ERR_FORMAT
+    # second entry writes its data over the first entry's transpose
+    clash = _desc(x=X + 0x100000, q=QT, qt=QT + 0x100000, amax=A + 64, sinv=SI + 64)
+    assert L.fp8_multi_cast_transpose(arr(good, clash), 2, 0, None, None) == CT_ERR_ALIAS
+    # second entry's amax is the first entry's scale_inv
+    clash = _desc(x=X + 0x100000, q=Q + 0x100000, qt=QT + 0x100000, amax=SI, sinv=SI + 64)
+    assert L.fp8_multi_cast_transpose(arr(good, clash), 2, 0, None, None) == CT_ERR_ALIAS
+    # empty entries are skipped: nothing to launch
+    e1, e2 = _desc(rows=0), _desc(cols=0, x=X + 0x100000, q=Q + 0x100000, qt=QT + 0x100000,
+                                  amax=A + 64, sinv=SI + 64)
+    assert L.fp8_multi_cast_transpose(arr(e1, e2), 2, 0, None, None) == CT_OK
+
+
+def test_device_error_needs_pointer(L):
+    assert L.ct_device_error(None, 0) == CT_ERR_NULL
+
+
+def test_python_binding_rejects_cpu_tensors():
+    import torch
+    x = torch.zeros(4, 4, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        ct.fp8_cast_transpose(x, torch.ones(1), torch.zeros(1), torch.zeros(1),
+                              torch.empty(16, dtype=torch.uint8), torch.empty(16, dtype=torch.uint8))

@@ -1,0 +1,143 @@
+"""GPU parity of fp8_cast_transpose and fp8_cast against the CPU oracle.
+
+Bit-exact comparison of FP8 bytes, transpose, amax and scale_inv, through
+the C ABI, on: every bf16 bit pattern at several scales, ragged and tiny
+shapes on both kernel paths (TMA-staged and general), misaligned buffers,
+the 256x512 N(0,1) matrix and the 4096x4096 weight-like matrix with its
+8-step delayed-scaling sequence.
+"""
+import numpy as np
+import pytest
+import torch
+
+import cast_transpose_gb300 as ct
+import oracle
+from cast_transpose_gb300 import workloads
+from gpu_util import Guarded, assert_same_cast, cast_transpose_gpu, f32_bits, scalar
+
+pytestmark = pytest.mark.gpu
+
+FMTS = [ct.E4M3, ct.E5M2]
+SCALES = [1.0, 2.0 ** -8, 2.0 ** 20, 3.7, 448.0 / 5.0, 2.0 ** 126, 1e-38]
+
+
+@pytest.fixture(autouse=True)
+def _no_device_error():
+    ct.device_error(clear=True)
+    yield
+    assert ct.device_error() == 0
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("scale", SCALES)
+def test_all_bf16_patterns(fmt, scale):
+    x_cpu = workloads.bf16_all_patterns()
+    scale = float(np.float32(scale))
+    got = cast_transpose_gpu(x_cpu.cuda(), scale, fmt)
+    ref = oracle.cast_transpose(x_cpu, scale, fmt)
+    assert_same_cast(got, ref)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_all_bf16_patterns_general_path(fmt):
+    # 2-byte offset of x: not 16-byte aligned, so the general kernel runs
+    x_cpu = workloads.bf16_all_patterns()
+    big = torch.empty(65536 + 1, dtype=torch.bfloat16, device="cuda")
+    big[1:] = x_cpu.cuda().reshape(-1)
+    x = big[1:].view(256, 256)
+    assert x.data_ptr() % 16 != 0
+    got = cast_transpose_gpu(x, 3.7, fmt)
+    assert_same_cast(got, oracle.cast_transpose(x_cpu, 3.7, fmt))
+
+
+SHAPES = [(1, 1), (1, 17), (17, 1), (2, 3), (33, 65), (127, 129), (17, 4097), (16, 16),
+          (16, 32), (128, 128), (144, 272), (256, 384), (130, 96), (4112, 48), (48, 8208),
+          (640, 1040), (1, 4096), (4096, 1)]
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("shape", SHAPES)
+def test_shapes(fmt, shape):
+    rows, cols = shape
+    x_cpu = workloads.normal_bf16(rows, cols, 60.0, 100 + rows * 7 + cols)
+    got = cast_transpose_gpu(x_cpu.cuda(), 2.5, fmt, amax_in=0.125)
+    assert_same_cast(got, oracle.cast_transpose(x_cpu, 2.5, fmt, amax_in=0.125))
+
+
+@pytest.mark.parametrize("out_offset", [1, 8])
+def test_misaligned_outputs(out_offset):
+    x_cpu = workloads.normal_bf16(256, 384, 1.0, 9)
+    got = cast_transpose_gpu(x_cpu.cuda(), 1.0, ct.E4M3, out_offset=out_offset)
+    assert_same_cast(got, oracle.cast_transpose(x_cpu, 1.0, ct.E4M3))
+
+
+def test_amax_is_max_merged_not_overwritten():
+    x_cpu = workloads.normal_bf16(256, 256, 1.0, 2)
+    got = cast_transpose_gpu(x_cpu.cuda(), 1.0, ct.E4M3, amax_in=1000.0)
+    assert got["amax"] == 1000.0
+
+
+def test_special_values_in_matrix():
+    x = torch.randn(128, 256).to(torch.bfloat16)
+    x[0, 0] = float("nan")
+    x[5, 7] = float("inf")
+    x[9, 9] = float("-inf")
+    x[10, 10] = -0.0
+    got = cast_transpose_gpu(x.cuda(), 1.0, ct.E5M2)
+    assert_same_cast(got, oracle.cast_transpose(x, 1.0, ct.E5M2))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("shape", [(256, 512), (33, 65), (144, 272)])
+def test_cast_only(fmt, shape):
+    rows, cols = shape
+    x_cpu = workloads.normal_bf16(rows, cols, 30.0, 4)
+    q = Guarded(rows * cols)
+    s, a, si = scalar(0.75), scalar(0.0), scalar(0.0)
+    ct.fp8_cast(x_cpu.cuda(), s, a, si, q.t, fmt)
+    torch.cuda.synchronize()
+    q.check()
+    ref = oracle.cast_transpose(x_cpu, 0.75, fmt)
+    assert np.array_equal(q.numpy().reshape(rows, cols), ref["q"])
+    assert f32_bits(a.item()) == f32_bits(ref["amax"])
+    assert f32_bits(si.item()) == f32_bits(ref["scale_inv"])
+
+
+def test_single_matrix_256x512():
+    x_cpu = workloads.single_matrix("cpu")
+    got = cast_transpose_gpu(x_cpu.cuda(), 1.0, ct.E4M3)
+    assert_same_cast(got, oracle.cast_transpose(x_cpu, 1.0, ct.E4M3))
+
+
+@pytest.mark.parametrize("hist_init", [0.0, 1.0])
+def test_weight_4096_eight_step_sequence(hist_init):
+    """4096x4096 N(0, 0.02), E4M3, history length 16, margin 0; steps cast
+    x * 2^k for k = -4..3, each followed by the scale update."""
+    L = 16
+    base = workloads.weight_matrix("cuda")
+    hist = torch.full((L, 1), hist_init, device="cuda")
+    hist[0] = 0.0
+    scale = scalar(1.0)
+    sinv = scalar(1.0)
+    h_ref = np.full((L, 1), hist_init, np.float32)
+    h_ref[0] = 0.0
+    s_ref = np.ones(1, np.float32)
+    si_ref = np.ones(1, np.float32)
+    rows, cols = base.shape
+    for k in workloads.WEIGHT_EXPONENTS:
+        x = workloads.weight_rescaled(base, k)
+        q, qt = ct.empty_outputs(x)
+        tensor_sinv = scalar(0.0)
+        ct.fp8_cast_transpose(x, scale, hist[0], tensor_sinv, q, qt, ct.E4M3)
+        ct.fp8_amax_and_scale_update(hist, scale, sinv, ct.E4M3, 0)
+        torch.cuda.synchronize()
+        x_cpu = x.cpu()
+        ref = oracle.cast_transpose(x_cpu, float(s_ref[0]), ct.E4M3, amax_in=float(h_ref[0, 0]))
+        assert np.array_equal(q.cpu().numpy(), ref["q"]), f"step k={k}: FP8 data differs"
+        assert np.array_equal(qt.cpu().numpy(), ref["qt"]), f"step k={k}: transpose differs"
+        assert f32_bits(tensor_sinv.item()) == f32_bits(ref["scale_inv"])
+        h_ref[0, 0] = ref["amax"]
+        h_ref, s_ref, si_ref = oracle.amax_and_scale_update(h_ref, s_ref, si_ref, ct.E4M3, 0)
+        assert np.array_equal(hist.cpu().numpy(), h_ref), f"step k={k}: history differs"
+        assert f32_bits(scale.item()) == f32_bits(s_ref[0]), (k, scale.item(), s_ref[0])
+        assert f32_bits(sinv.item()) == f32_bits(si_ref[0])

@@ -1,0 +1,88 @@
+"""GPU parity of fp8_dbias_cast_transpose against the CPU oracle.
+
+FP8 bytes, transpose, amax and scale_inv bit-exact; db within
+|db - db_ref| <= 1e-5 * sum_i |dy[i, j]| + 1e-6 (db_ref accumulated in
+double by the oracle).  Includes the 8192x12288 gradient-like dy (N(0, 1e-3)
+with 0.01% +-5.0 outliers, E5M2) for two steps: scale 1, then the scale
+the update derives from the first step's amax.
+"""
+import numpy as np
+import pytest
+import torch
+
+import cast_transpose_gb300 as ct
+import oracle
+from cast_transpose_gb300 import workloads
+from gpu_util import Guarded, dbias_tolerance_ok, f32_bits, scalar
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _no_device_error():
+    ct.device_error(clear=True)
+    yield
+    assert ct.device_error() == 0
+
+
+def run_dbias(dy, scale, fmt, amax_in=0.0):
+    rows, cols = dy.shape
+    n = rows * cols
+    q, qt = Guarded(n), Guarded(n)
+    db = Guarded(cols, dtype=torch.float32)
+    ws = torch.empty(ct.dbias_workspace_size(rows, cols), dtype=torch.uint8, device="cuda")
+    ws.fill_(0x7F)   # garbage: the kernel must not depend on its contents
+    s, a, si = scalar(scale), scalar(amax_in), scalar(0.0)
+    ct.fp8_dbias_cast_transpose(dy, s, a, si, q.t, qt.t, db.t, ws, fmt)
+    torch.cuda.synchronize()
+    for g in (q, qt, db):
+        g.check()
+    return {"q": q.numpy().reshape(rows, cols), "qt": qt.numpy().reshape(cols, rows),
+            "db": db.numpy(), "amax": a.item(), "scale_inv": si.item()}
+
+
+def check(got, x_cpu, scale, fmt, amax_in=0.0):
+    ref = oracle.cast_transpose(x_cpu, scale, fmt, amax_in=amax_in)
+    assert np.array_equal(got["q"], ref["q"]), "FP8 data differs"
+    assert np.array_equal(got["qt"], ref["qt"]), "transpose differs"
+    assert f32_bits(got["amax"]) == f32_bits(ref["amax"])
+    assert f32_bits(got["scale_inv"]) == f32_bits(ref["scale_inv"])
+    db_ref = oracle.dbias(x_cpu)
+    assert dbias_tolerance_ok(got["db"], db_ref, x_cpu), \
+        np.max(np.abs(got["db"] - db_ref))
+    return ref
+
+
+SHAPES = [(1, 1), (3, 17), (128, 128), (127, 129), (129, 256), (1000, 48), (2048, 272),
+          (4112, 1040)]
+
+
+@pytest.mark.parametrize("fmt", [ct.E4M3, ct.E5M2])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_shapes(fmt, shape):
+    rows, cols = shape
+    x_cpu = workloads.gradient_matrix("cpu", rows, cols, std=1e-3, outlier_fraction=1e-3)
+    check(run_dbias(x_cpu.cuda(), 1.0, fmt), x_cpu, 1.0, fmt)
+
+
+def test_deterministic():
+    x = workloads.gradient_matrix("cuda", 2048, 1024)
+    a = run_dbias(x, 1.0, ct.E5M2)
+    b = run_dbias(x, 1.0, ct.E5M2)
+    assert np.array_equal(a["db"].view(np.uint32), b["db"].view(np.uint32))
+
+
+def test_gradient_8192x12288_two_steps():
+    dy = workloads.gradient_matrix("cuda")
+    x_cpu = dy.cpu()
+    assert int((x_cpu.float().abs() == 5.0).sum()) == round(1e-4 * dy.numel())
+    got = run_dbias(dy, 1.0, ct.E5M2)
+    ref = check(got, x_cpu, 1.0, ct.E5M2)
+    assert ref["amax"] == 5.0
+    # second step with the scale the update derives (57344 / 5)
+    hist = np.zeros((16, 1), np.float32)
+    hist[0, 0] = ref["amax"]
+    _, s, _ = oracle.amax_and_scale_update(hist, np.ones(1, np.float32), np.ones(1, np.float32),
+                                           ct.E5M2, 0)
+    got2 = run_dbias(dy, float(s[0]), ct.E5M2)
+    check(got2, x_cpu, float(s[0]), ct.E5M2)

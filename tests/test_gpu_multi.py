@@ -1,0 +1,124 @@
+"""GPU parity of fp8_multi_cast_transpose (one launch over a tensor list).
+
+Small lists are compared in full; the 48-tensor list (12 each of
+6144x12288, 12288x6144, 18432x6144, 6144x24576, N(0, 0.02), two all-zero and
+two rescaled to max|x| = 1e-30) is checked on sampled row blocks against the
+oracle, with its full amaxes from the oracle, q^T == q checked on the GPU for
+every tensor, and the 48-tensor scale update (zero-amax guard) compared
+exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import cast_transpose_gb300 as ct
+import oracle
+from cast_transpose_gb300 import workloads
+from gpu_util import Guarded, f32_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _no_device_error():
+    ct.device_error(clear=True)
+    yield
+    assert ct.device_error() == 0
+
+
+def _run_list(xs, scales_val, fmt, misalign=()):
+    n = len(xs)
+    scales = torch.tensor(scales_val, dtype=torch.float32, device="cuda")
+    amax = torch.zeros(n, device="cuda")
+    sinv = torch.zeros(n, device="cuda")
+    outs, outs_t = [], []
+    for i, x in enumerate(xs):
+        m = x.numel()
+        outs.append(Guarded(m, offset=1 if i in misalign else 0))
+        outs_t.append(Guarded(m))
+    ct.fp8_multi_cast_transpose(xs, [scales[i:i + 1] for i in range(n)],
+                                [amax[i:i + 1] for i in range(n)],
+                                [sinv[i:i + 1] for i in range(n)],
+                                [o.t for o in outs], [o.t for o in outs_t], fmt)
+    torch.cuda.synchronize()
+    return outs, outs_t, amax.cpu().numpy(), sinv.cpu().numpy()
+
+
+@pytest.mark.parametrize("fmt", [ct.E4M3, ct.E5M2])
+def test_small_mixed_list(fmt):
+    shapes = [(256, 384), (33, 65), (128, 128), (0, 16), (144, 272), (1, 1), (4096, 16),
+              (16, 4096)]
+    xs_cpu = [workloads.normal_bf16(r, c, 40.0, 50 + i) for i, (r, c) in enumerate(shapes)]
+    scales = [1.0, 0.5, 2.0, 1.0, 3.0, 1.0, 0.25, 8.0]
+    outs, outs_t, amax, sinv = _run_list([x.cuda() for x in xs_cpu], scales, fmt, misalign=(2,))
+    for i, x in enumerate(xs_cpu):
+        r, c = x.shape
+        outs[i].check()
+        outs_t[i].check()
+        if x.numel() == 0:
+            assert amax[i] == 0.0 and sinv[i] == 0.0
+            continue
+        ref = oracle.cast_transpose(x, scales[i], fmt)
+        assert np.array_equal(outs[i].numpy().reshape(r, c), ref["q"]), i
+        assert np.array_equal(outs_t[i].numpy().reshape(c, r), ref["qt"]), i
+        assert f32_bits(amax[i]) == f32_bits(ref["amax"]), i
+        assert f32_bits(sinv[i]) == f32_bits(ref["scale_inv"]), i
+
+
+def test_list_longer_than_one_launch():
+    xs_cpu = [workloads.normal_bf16(16 * (1 + i % 5), 32 * (1 + i % 3), 1.0, 300 + i)
+              for i in range(70)]
+    scales = [float(1 + i % 4) for i in range(70)]
+    outs, outs_t, amax, sinv = _run_list([x.cuda() for x in xs_cpu], scales, ct.E4M3)
+    for i, x in enumerate(xs_cpu):
+        r, c = x.shape
+        ref = oracle.cast_transpose(x, scales[i], ct.E4M3)
+        assert np.array_equal(outs[i].numpy().reshape(r, c), ref["q"]), i
+        assert np.array_equal(outs_t[i].numpy().reshape(c, r), ref["qt"]), i
+        assert f32_bits(amax[i]) == f32_bits(ref["amax"]), i
+
+
+def test_multi_48_tensor_list_with_update():
+    n = workloads.MULTI_COUNT
+    xs = workloads.multi_list("cuda")
+    scales = torch.ones(n, device="cuda")
+    L = 16
+    hist = torch.zeros(L, n, device="cuda")
+    tsinv = torch.zeros(n, device="cuda")
+    outs = [torch.empty(x.numel(), dtype=torch.uint8, device="cuda") for x in xs]
+    outs_t = [torch.empty(x.numel(), dtype=torch.uint8, device="cuda") for x in xs]
+    ct.fp8_multi_cast_transpose(xs, [scales[i:i + 1] for i in range(n)],
+                                [hist[0, i:i + 1] for i in range(n)],
+                                [tsinv[i:i + 1] for i in range(n)], outs, outs_t, ct.E4M3)
+    amax_gpu = hist[0].cpu().numpy().copy()
+    recipe_sinv = torch.ones(n, device="cuda")
+    ct.fp8_amax_and_scale_update(hist, scales, recipe_sinv, ct.E4M3, 0)
+    torch.cuda.synchronize()
+
+    rng = np.random.default_rng(0)
+    amax_ref = np.zeros(n, np.float32)
+    for i, x in enumerate(xs):
+        r, c = x.shape
+        q = outs[i].view(r, c)
+        qt = outs_t[i].view(c, r)
+        assert torch.equal(qt, q.t()), f"tensor {i}: transpose is not q^T"
+        x_cpu = x.cpu()
+        amax_ref[i] = oracle.amax(x_cpu)
+        assert f32_bits(amax_gpu[i]) == f32_bits(amax_ref[i]), (i, amax_gpu[i], amax_ref[i])
+        # sampled 128-row blocks (first, last, one random) through the oracle
+        for r0 in {0, r - 128, int(rng.integers(0, r // 128)) * 128}:
+            ref = oracle.cast_transpose(x_cpu[r0:r0 + 128], 1.0, ct.E4M3, want_qt=False)
+            assert np.array_equal(q[r0:r0 + 128].cpu().numpy(), ref["q"]), (i, r0)
+        assert tsinv[i].item() == 1.0
+    assert np.all(amax_ref[list(workloads.MULTI_ZERO)] == 0.0)
+    tiny = amax_ref[list(workloads.MULTI_TINY)]
+    assert np.all((tiny > 0) & (tiny < 1.1e-30))
+
+    h_ref = np.zeros((L, n), np.float32)
+    h_ref[0] = amax_ref
+    h_ref, s_ref, si_ref = oracle.amax_and_scale_update(h_ref, np.ones(n, np.float32),
+                                                        np.ones(n, np.float32), ct.E4M3, 0)
+    assert np.array_equal(hist.cpu().numpy(), h_ref)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(recipe_sinv.cpu().numpy().view(np.uint32), si_ref.view(np.uint32))
+    assert np.all(s_ref[list(workloads.MULTI_ZERO)] == 1.0)     # amax 0: scale kept

@@ -60,6 +60,8 @@ def test_amax_matches_torch_and_merges(oracle_lib):
     assert oracle.cast_transpose(x, 1.0, oracle.E4M3)["amax"] == np.float32(ref)
     assert oracle.cast_transpose(x, 1.0, oracle.E4M3, amax_in=1e6)["amax"] == np.float32(1e6)
     assert oracle.cast_transpose(x, 1.0, oracle.E4M3, amax_in=0.5)["amax"] == np.float32(ref)
+    assert oracle.amax(x) == np.float32(ref)
+    assert oracle.amax(x, 7.0) == np.float32(max(ref, 7.0))
     y = x.clone()
     y[3, 4] = float("nan")
     assert np.isnan(oracle.cast_transpose(y, 1.0, oracle.E4M3)["amax"])
