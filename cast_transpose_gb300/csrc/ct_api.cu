@@ -119,8 +119,9 @@ void fill_tensor(FastTensor& t, const void* out, const void* out_t, const float*
     t.rows = rows;
     t.cols = cols;
     t.tile_cols = (cols + ct::kTileCols - 1) / ct::kTileCols;
+    t.tile_rows = (rows + ct::kTileRows - 1) / ct::kTileRows;
     t.tile_begin = tile_begin;
-    t.tile_end = tile_begin + ((rows + ct::kTileRows - 1) / ct::kTileRows) * t.tile_cols;
+    t.tile_end = tile_begin + t.tile_rows * t.tile_cols;
 }
 
 int cast_impl(const void* x, int64_t rows, int64_t cols, const float* scale, float* amax,

@@ -28,6 +28,18 @@ __device__ __forceinline__ uint32_t cvt_fp8x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Two IEEE fp32 products a*s, b*s (round to nearest even, no flush to
+// zero) with one packed f32x2 multiply of the sm_100 family.
+__device__ __forceinline__ void mul2_rn(float a, float b, float s, float& ra, float& rb) {
+    asm("{\n\t.reg .b64 ta, ts, td;\n\t"
+        "mov.b64 ta, {%2, %3};\n\t"
+        "mov.b64 ts, {%4, %4};\n\t"
+        "mul.rn.f32x2 td, ta, ts;\n\t"
+        "mov.b64 {%0, %1}, td;\n\t}"
+        : "=f"(ra), "=f"(rb)
+        : "f"(a), "f"(b), "f"(s));
+}
+
 // Cast 8 bf16 (one 16-byte vector) to 8 FP8 codes (two 32-bit words, byte i
 // = element i).
 template <int FMT>
@@ -36,12 +48,23 @@ __device__ __forceinline__ uint2 cast8(const uint4& v, float scale) {
     uint32_t h[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const float a = __fmul_rn(bf16_lo(w[e]), scale);
-        const float b = __fmul_rn(bf16_hi(w[e]), scale);
+        float a, b;
+        mul2_rn(bf16_lo(w[e]), bf16_hi(w[e]), scale, a, b);
         h[e] = cvt_fp8x2<FMT>(a, b);
     }
     return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
 }
+
+// ---- programmatic dependent launch ----------------------------------------
+// Every kernel of the library is launched with programmatic stream
+// serialisation allowed.  It first lets the next kernel in the stream be
+// scheduled (that kernel will itself wait below), then waits until every
+// kernel it depends on has completed and its memory is visible, before it
+// reads anything.  With an ordinary predecessor both are no-ops.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---- shared-memory addresses, timers ----------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -97,6 +120,27 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
 }
 
+// The same, but also gives up as soon as *abort becomes nonzero.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  const volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0 && (*abort || globaltimer_ns() - t0 > kWaitLimitNs)) return false;
+    }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Barrier among the `count` threads of the consumer warps only (named
+// barrier 1; barrier 0 is __syncthreads).
+__device__ __forceinline__ void consumer_sync(int count) {
+    asm volatile("bar.sync 1, %0;" ::"r"(count) : "memory");
+}
+
 // ---- TMA ---------------------------------------------------------------------
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t pol;
@@ -132,9 +176,11 @@ __device__ __forceinline__ void transpose4x4(uint32_t r0, uint32_t r1, uint32_t 
 }
 
 // Max of the two bf16 magnitudes (sign cleared) of a packed pair, kept as a
-// pair so that one SIMD max per word suffices.
+// pair: one AND and one native 16x2 unsigned max per word.
 __device__ __forceinline__ uint32_t absmax_pair(uint32_t acc, uint32_t w) {
-    return __vmaxu2(acc, w & 0x7FFF7FFFu);
+    uint32_t r;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(acc), "r"(w & 0x7FFF7FFFu));
+    return r;
 }
 
 // Collapse a pair accumulator into the fp32 bit pattern of the larger

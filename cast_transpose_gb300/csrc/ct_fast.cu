@@ -8,18 +8,23 @@
 //
 // Design (HBM-bound stream, 4 bytes of traffic per element, no contraction):
 //   * persistent CTAs, one per SM, walk 128x128 tiles round-robin; tile t of
-//     CTA b is b + k * gridDim.x, so concurrently running CTAs touch
-//     neighbouring tiles and whole rows of x stream through DRAM pages;
-//   * one thread issues 2-D TMA loads of 32 KB bf16 tiles into a ring of
-//     STAGES shared-memory buffers, each guarded by an mbarrier; the loads
-//     carry an L2 evict-first hint since x is read once;
+//     CTA b is b + k * gridDim.x in an order of bands of 8 tile rows,
+//     column-major inside a band, so the tiles in flight at one time form a
+//     compact block of x, q and qT;
+//   * the producer maps tile indices to coordinates and hands them to the
+//     consumers in shared memory next to the staged tile, off their path;
+//   * a dedicated producer warp (one elected lane) issues 2-D TMA loads of
+//     32 KB bf16 tiles into a ring of STAGES shared-memory buffers: a "full"
+//     mbarrier per stage completes on the TMA transaction bytes, an "empty"
+//     mbarrier per stage completes when all consumer warps have read it; the
+//     loads carry an L2 evict-first hint since x is read once;
 //   * pass 1 (all 256 threads): each thread reads 16-byte row vectors of the
 //     staged tile (8 threads cover 128 contiguous bytes: no bank conflict),
 //     converts 8 bf16 to 8 FP8 codes (fp32 multiply, cvt.rn.satfinite),
 //     stores them straight to q (16 threads write one full 128-byte line) and
 //     into an XOR-swizzled FP8 copy of the tile in shared memory; it also
 //     keeps the running amax and, for dbias, per-column fp32 sums;
-//   * one CTA barrier per tile; after it the stage is refilled by TMA;
+//   * one barrier per tile among the consumer warps only (named barrier 1);
 //   * pass 2: each thread gathers a 16-row x 4-column byte block from the
 //     swizzled copy (conflict-free), transposes it with byte permutes and
 //     writes four 16-byte vectors of qT (8 threads write one 128-byte line);
@@ -42,29 +47,83 @@ namespace {
 
 constexpr int kStageBytes = kTileRows * kTileCols * 2;   // bf16 tile
 constexpr int kSqBytes = kTileRows * kTileCols;          // FP8 copy
-constexpr int kColsumFloats = 8 * kTileCols;              // [warp][col]
+
+// Threads per CTA of the TMA kernels (256 or 512; compile-time constant).
+#ifndef CT_THREADS
+#define CT_THREADS 256
+#endif
+constexpr int kFastThreads = CT_THREADS;
+static_assert(kFastThreads == 256 || kFastThreads == 512, "256 or 512 threads");
+constexpr int kWarps = kFastThreads / 32;
+constexpr int kColsumFloats = kWarps * kTileCols;         // [warp][col]
+
+// Shared-memory layout of the FP8 copy of a tile: 128 rows of 32 words (4
+// FP8 codes each); word wd of row r lives at wd ^ swz(r).  The XOR spreads
+// the 8 row blocks that pass 2 reads at once over all 32 banks, and keeps
+// the two words of every 8-byte pass-1 store adjacent.
+__device__ __forceinline__ int swz(int r) { return 2 * ((r >> 3) & 15); }
+
+// Where a staged tile came from.  Written by the producer thread before it
+// arms the stage's mbarrier, read by the consumers after the barrier phase
+// completes (the arrive releases, the wait acquires), so only one thread
+// ever maps tile indices to coordinates.
+struct StageInfo {
+    int32_t tensor;        // index into p.t / p.map
+    int32_t last;          // 1: this CTA's last tile of that tensor
+    int32_t rt;            // tile row
+    int32_t ct;            // tile column
+};
 
 template <int STAGES, bool WRITE_T, bool DBIAS>
 struct SmemLayout {
     static constexpr int stage_off = 0;
     static constexpr int sq_off = STAGES * kStageBytes;
     static constexpr int colsum_off = sq_off + (WRITE_T ? 2 * kSqBytes : 0);
-    static constexpr int mbar_off = colsum_off + (DBIAS ? 2 * kColsumFloats * 4 : 0);
-    static constexpr int amax_off = mbar_off + STAGES * 8;
+    static constexpr int full_off = colsum_off + (DBIAS ? 2 * kColsumFloats * 4 : 0);
+    static constexpr int empty_off = full_off + STAGES * 8;
+    static constexpr int info_off = empty_off + STAGES * 8;
+    static constexpr int amax_off = info_off + STAGES * int(sizeof(StageInfo));
     static constexpr int abort_off = amax_off + 8;
     static constexpr int bytes = abort_off + 8 + 128;   // +128: base alignment slack
 };
 
-template <int NT, int FMT, int STAGES, bool WRITE_T, bool DBIAS>
-__global__ void __launch_bounds__(kThreads, 1)
+// Order of the tiles of one tensor: bands of kBand tile rows, column-major
+// inside a band, so that the ~150 tiles in flight at once form a block about
+// kBand tiles tall.  The transposed output then receives kBand x 128 bytes
+// of every row it touches at the same time, not 128 scattered bytes.
+#ifndef CT_BAND
+#define CT_BAND 8
+#endif
+constexpr uint32_t kBand = CT_BAND;
+
+__device__ __forceinline__ void tile_coords(uint32_t local, uint32_t tile_rows, uint32_t tile_cols,
+                                            int32_t& rt, int32_t& ct) {
+    const uint32_t band = local / (kBand * tile_cols);
+    const uint32_t rem = tile_rows - band * kBand;
+    const uint32_t h = rem < kBand ? rem : kBand;
+    const uint32_t idx = local - band * kBand * tile_cols;
+    const uint32_t c = idx / h;
+    ct = static_cast<int32_t>(c);
+    rt = static_cast<int32_t>(band * kBand + (idx - c * h));
+}
+
+// Block: kFastThreads consumer threads (warps 0 .. kWarps-1) plus one
+// producer warp (warp kWarps) whose lane 0 drives the TMA pipeline.
+constexpr int kBlockThreads = kFastThreads + 32;
+
+template <int NT, int FMT, int STAGES, int MINB, bool WRITE_T, bool DBIAS>
+__global__ void __launch_bounds__(kBlockThreads, MINB)
     fast_cast_transpose_kernel(const __grid_constant__ FastParams<NT> p) {
     using L = SmemLayout<STAGES, WRITE_T, DBIAS>;
-    if (p.noop != nullptr && *p.noop != 0.0f) return;
+    // Rows of the staged tile loaded per batch in pass 1: all at once for the
+    // most loads in flight, 4 when registers are tight.
+    constexpr int kBatch = (DBIAS && (MINB > 1 || kFastThreads == 512)) ? 4 : 8 * 256 / kFastThreads;
+    dev::pdl_launch_dependents();
 
-    const int64_t first = blockIdx.x;
-    const int64_t G = gridDim.x;
+    const uint32_t first = blockIdx.x;
+    const uint32_t G = gridDim.x;
     if (first >= p.total_tiles) return;
-    const int64_t my_tiles = (p.total_tiles - first + G - 1) / G;
+    const uint32_t my_tiles = static_cast<uint32_t>((p.total_tiles - first + G - 1) / G);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -72,7 +131,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* stages = smem + L::stage_off;
     uint8_t* sq = smem + L::sq_off;
     float* colsum = reinterpret_cast<float*>(smem + L::colsum_off);
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + L::mbar_off);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::full_off);
+    uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L::empty_off);
+    StageInfo* info = reinterpret_cast<StageInfo*>(smem + L::info_off);
     unsigned* s_amax = reinterpret_cast<unsigned*>(smem + L::amax_off);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::abort_off);
 
@@ -80,96 +141,145 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = tid & 31;
     const int warp = tid >> 5;
 
-    // ---- producer state (thread 0 only) ------------------------------------
-    int icur = 0;            // tensor of the next tile to load
-    int64_t issued = 0;      // tiles of this CTA whose load has been issued
-    uint64_t policy = 0;
-
-    auto issue = [&](int64_t kk) {
-        const int64_t tile = first + kk * G;
-        while (tile >= p.t[icur].tile_end) ++icur;
-        const FastTensor& T = p.t[icur];
-        const int64_t local = tile - T.tile_begin;
-        const int64_t rt = local / T.tile_cols;
-        const int64_t ctl = local - rt * T.tile_cols;
-        const int s = static_cast<int>(kk % STAGES);
-        dev::mbar_arrive_expect_tx(&mbar[s], kStageBytes);
-        dev::tma_load_2d(stages + s * kStageBytes, &p.map[icur],
-                         static_cast<int32_t>(ctl * kTileCols),
-                         static_cast<int32_t>(rt * kTileRows), &mbar[s], policy);
-    };
-
     if (tid == 0) {
-        for (int s = 0; s < STAGES; ++s) dev::mbar_init(&mbar[s], 1);
+        for (int s = 0; s < STAGES; ++s) {
+            dev::mbar_init(&full[s], 1);           // producer's arrive + TMA bytes
+            dev::mbar_init(&empty[s], kWarps);     // one arrive per consumer warp
+        }
         s_amax[0] = 0;
         s_amax[1] = 0;
         *s_abort = 0;
         dev::fence_barrier_init();
-        policy = dev::policy_evict_first();
-        for (; issued < my_tiles && issued < STAGES; ++issued) issue(issued);
     }
     __syncthreads();
+    // Everything above touched only shared memory and parameters; from here
+    // on global memory written by the preceding kernel may be read.
+    dev::pdl_wait();
+    if (p.noop != nullptr && *p.noop != 0.0f) return;
 
-    // ---- consumer state ----------------------------------------------------
-    int cur = 0;                // tensor of the current tile
+    // =============================== producer ================================
+    if (warp == kWarps) {
+        if (lane != 0) return;
+        const uint64_t policy = dev::policy_evict_first();
+        int icur = 0;
+        uint32_t issued = 0;
+        for (; issued < my_tiles; ++issued) {
+            const uint32_t kk = issued;
+            const int s = static_cast<int>(kk % STAGES);
+            if (kk >= STAGES &&
+                !dev::mbar_wait_bounded(&empty[s], ((kk / STAGES) - 1) & 1u, s_abort))
+                break;
+            const int64_t tile = int64_t(first) + int64_t(kk) * G;
+            while (tile >= p.t[icur].tile_end) ++icur;
+            const FastTensor& T = p.t[icur];
+            StageInfo inf;
+            inf.tensor = icur;
+            inf.last = (kk + 1 == my_tiles) || (tile + G >= T.tile_end);
+            tile_coords(static_cast<uint32_t>(tile - T.tile_begin),
+                        static_cast<uint32_t>(T.tile_rows), static_cast<uint32_t>(T.tile_cols),
+                        inf.rt, inf.ct);
+            info[s] = inf;
+            dev::mbar_arrive_expect_tx(&full[s], kStageBytes);
+            dev::tma_load_2d(stages + s * kStageBytes, &p.map[icur], inf.ct * kTileCols,
+                             inf.rt * kTileRows, &full[s], policy);
+        }
+        if (issued < my_tiles) {
+            // The consumers stopped (or never released a stage): flag it.
+            *s_abort = 1;
+            atomicOr(&g_device_error, kErrWaitTimeout);
+        }
+        // Stay until the loads still in flight into this CTA's shared memory
+        // have landed (bounded), whether or not the consumers still want them.
+        const uint32_t lo = issued > STAGES ? issued - STAGES : 0;
+        for (uint32_t kk = lo; kk < issued; ++kk)
+            (void)dev::mbar_wait_bounded(&full[kk % STAGES], (kk / STAGES) & 1u);
+        return;
+    }
+
+    // =============================== consumers ===============================
+    int cur = -1;               // tensor of the current run, and its fields:
+    float scale = 0.0f;         // loaded once per run, not once per tile
+    int64_t rows = 0, cols = 0;
+    uint8_t* out = nullptr;
+    uint8_t* out_t = nullptr;
     uint32_t amax_pair = 0;     // running bf16 magnitude max (pair form)
 
-    // pass-1 mapping: column chunk c (8 columns), rows rg + 16*it
+    // pass-1 mapping: column chunk c (8 columns), rows rg + kRowStep*it
+    constexpr int kRowStep = kFastThreads / 16;           // 16 or 32
+    constexpr int kRowsPerThread = kTileRows / kRowStep;  // 8 or 4
     const int c = tid & 15;
     const int rg = tid >> 4;
-    // pass-2 mapping: 16-row block b, 4-column word w
-    const int b = lane & 7;
-    const int w = warp * 4 + (lane >> 3);
+    // pass-2 mapping: block b of kBlockRows rows, 4-column word w
+    constexpr int kBlockRows = kFastThreads == 256 ? 16 : 8;
+    constexpr int kBlocks = kTileRows / kBlockRows;       // 8 or 16
+    const int b = lane % kBlocks;
+    const int w = warp * (32 / kBlocks) + lane / kBlocks;
 
-    for (int64_t k = 0; k < my_tiles; ++k) {
-        const int64_t tile = first + k * G;
-        while (tile >= p.t[cur].tile_end) ++cur;
-        const FastTensor& T = p.t[cur];
-        const int64_t rows = T.rows, cols = T.cols;
-        const int64_t local = tile - T.tile_begin;
-        const int64_t rt = local / T.tile_cols;
-        const int64_t row0 = rt * kTileRows;
-        const int64_t col0 = (local - rt * T.tile_cols) * kTileCols;
-        const float scale = *T.scale;
+    for (uint32_t k = 0; k < my_tiles; ++k) {
         const int s = static_cast<int>(k % STAGES);
-        const uint32_t parity = static_cast<uint32_t>((k / STAGES) & 1);
-        const int sb = static_cast<int>(k & 1);
+        const int sb = static_cast<int>(k & 1u);
         uint8_t* sqb = sq + sb * kSqBytes;
+        int64_t row0 = 0, col0 = 0, rt = 0;
+        bool last = false, first_tile = false;
 
         float cs[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) cs[j] = 0.0f;
 
-        if (!dev::mbar_wait_bounded(&mbar[s], parity)) {
+        if (!dev::mbar_wait_bounded(&full[s], (k / STAGES) & 1u, s_abort)) {
             *s_abort = 1;
         } else {
+            const StageInfo inf = info[s];
+            if (inf.tensor != cur) {
+                cur = inf.tensor;
+                scale = *p.t[cur].scale;
+                rows = p.t[cur].rows;
+                cols = p.t[cur].cols;
+                out = p.t[cur].out;
+                out_t = p.t[cur].out_t;
+            }
+            rt = inf.rt;
+            row0 = int64_t(inf.rt) * kTileRows;
+            col0 = int64_t(inf.ct) * kTileCols;
+            last = inf.last != 0;
+            first_tile = inf.rt == 0 && inf.ct == 0;
+
             // ---------------- pass 1 ----------------
             const uint8_t* in = stages + s * kStageBytes;
-            uint4 v[8];
-#pragma unroll
-            for (int it = 0; it < 8; ++it)
-                v[it] = *reinterpret_cast<const uint4*>(in + (rg + 16 * it) * (kTileCols * 2) + c * 16);
             const bool col_ok = col0 + 8 * c < cols;
-            uint8_t* qrow = T.out + row0 * cols + col0 + 8 * c;
+            uint8_t* qrow = out + row0 * cols + col0 + 8 * c;
 #pragma unroll
-            for (int it = 0; it < 8; ++it) {
-                const int r = rg + 16 * it;
-                amax_pair = dev::absmax_pair(amax_pair, v[it].x);
-                amax_pair = dev::absmax_pair(amax_pair, v[it].y);
-                amax_pair = dev::absmax_pair(amax_pair, v[it].z);
-                amax_pair = dev::absmax_pair(amax_pair, v[it].w);
-                if constexpr (DBIAS) {
-                    cs[0] += dev::bf16_lo(v[it].x); cs[1] += dev::bf16_hi(v[it].x);
-                    cs[2] += dev::bf16_lo(v[it].y); cs[3] += dev::bf16_hi(v[it].y);
-                    cs[4] += dev::bf16_lo(v[it].z); cs[5] += dev::bf16_hi(v[it].z);
-                    cs[6] += dev::bf16_lo(v[it].w); cs[7] += dev::bf16_hi(v[it].w);
+            for (int it0 = 0; it0 < kRowsPerThread; it0 += kBatch) {
+                uint4 v[kBatch];
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j)
+                    v[j] = *reinterpret_cast<const uint4*>(
+                        in + (rg + kRowStep * (it0 + j)) * (kTileCols * 2) + c * 16);
+                if (it0 + kBatch == kRowsPerThread) {
+                    // every read of this stage has been issued and its value is
+                    // in a register: hand the stage back to the producer
+                    __syncwarp();
+                    if (lane == 0) dev::mbar_arrive(&empty[s]);
                 }
-                const uint2 q8 = dev::cast8<FMT>(v[it], scale);
-                if (col_ok && row0 + r < rows)
-                    *reinterpret_cast<uint2*>(qrow + r * cols) = q8;
-                if constexpr (WRITE_T) {
-                    // word index 2c of row r, XOR-swizzled by 4 * (r / 16)
-                    *reinterpret_cast<uint2*>(sqb + r * kTileCols + ((2 * c) ^ (4 * it)) * 4) = q8;
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int it = it0 + j;
+                    const int r = rg + kRowStep * it;
+                    amax_pair = dev::absmax_pair(amax_pair, v[j].x);
+                    amax_pair = dev::absmax_pair(amax_pair, v[j].y);
+                    amax_pair = dev::absmax_pair(amax_pair, v[j].z);
+                    amax_pair = dev::absmax_pair(amax_pair, v[j].w);
+                    if constexpr (DBIAS) {
+                        cs[0] += dev::bf16_lo(v[j].x); cs[1] += dev::bf16_hi(v[j].x);
+                        cs[2] += dev::bf16_lo(v[j].y); cs[3] += dev::bf16_hi(v[j].y);
+                        cs[4] += dev::bf16_lo(v[j].z); cs[5] += dev::bf16_hi(v[j].z);
+                        cs[6] += dev::bf16_lo(v[j].w); cs[7] += dev::bf16_hi(v[j].w);
+                    }
+                    const uint2 q8 = dev::cast8<FMT>(v[j], scale);
+                    if (col_ok && row0 + r < rows)
+                        *reinterpret_cast<uint2*>(qrow + r * cols) = q8;
+                    if constexpr (WRITE_T)   // words 2c, 2c+1 of row r
+                        *reinterpret_cast<uint2*>(sqb + r * kTileCols + ((2 * c) ^ swz(r)) * 4) = q8;
                 }
             }
             if constexpr (DBIAS) {
@@ -185,57 +295,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         // End of this CTA's run over the current tensor: fold the amax.
-        const bool last_of_run = (k + 1 == my_tiles) || (tile + G >= T.tile_end);
-        if (last_of_run) {
+        if (last) {
             const unsigned m = __reduce_max_sync(0xFFFFFFFFu, dev::pair_to_f32_bits(amax_pair));
             if (lane == 0 && m != 0) atomicMax(&s_amax[sb], m);
             amax_pair = 0;
         }
 
-        __syncthreads();
-
+        dev::consumer_sync(kFastThreads);
         if (*s_abort) {
-            if (tid == 0) {
-                atomicOr(&g_device_error, kErrWaitTimeout);
-                for (int64_t kk = k; kk < issued; ++kk)
-                    (void)dev::mbar_wait_bounded(&mbar[kk % STAGES],
-                                                 static_cast<uint32_t>((kk / STAGES) & 1));
-            }
-            return;
+            if (tid == 0) atomicOr(&g_device_error, kErrWaitTimeout);
+            return;   // the producer drains its own loads
         }
 
         if (tid == 0) {
-            if (issued < my_tiles) {   // refill the stage pass 1 just released
-                issue(issued);
-                ++issued;
-            }
-            if (last_of_run) {
+            if (last) {
                 const unsigned m = s_amax[sb];
                 s_amax[sb] = 0;
-                if (m != 0) atomicMax(reinterpret_cast<unsigned*>(T.amax), m);
+                if (m != 0) atomicMax(reinterpret_cast<unsigned*>(p.t[cur].amax), m);
             }
-            if (local == 0) *T.scale_inv = __fdiv_rn(1.0f, scale);
+            if (first_tile) *p.t[cur].scale_inv = __fdiv_rn(1.0f, scale);
         }
 
         // ---------------- pass 2 ----------------
         if constexpr (WRITE_T) {
             const uint32_t* sq32 = reinterpret_cast<const uint32_t*>(sqb);
-            uint32_t rw[16];
+            uint32_t rw[kBlockRows];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) rw[j] = sq32[(16 * b + j) * (kTileCols / 4) + (w ^ (4 * b))];
-            uint32_t o[4][4];
+            for (int j = 0; j < kBlockRows; ++j) {
+                const int r = kBlockRows * b + j;
+                rw[j] = sq32[r * (kTileCols / 4) + (w ^ swz(r))];
+            }
+            constexpr int kGroups = kBlockRows / 4;
+            uint32_t o[4][kGroups];
 #pragma unroll
-            for (int g = 0; g < 4; ++g)
+            for (int g = 0; g < kGroups; ++g)
                 dev::transpose4x4(rw[4 * g], rw[4 * g + 1], rw[4 * g + 2], rw[4 * g + 3], o[0][g],
                                   o[1][g], o[2][g], o[3][g]);
-            const int64_t row = row0 + 16 * b;
+            const int64_t row = row0 + kBlockRows * b;
             if (row < rows) {
 #pragma unroll
                 for (int kq = 0; kq < 4; ++kq) {
                     const int64_t col = col0 + 4 * w + kq;
-                    if (col < cols)
-                        *reinterpret_cast<uint4*>(T.out_t + col * rows + row) =
+                    if (col >= cols) continue;
+                    if constexpr (kGroups == 4)
+                        *reinterpret_cast<uint4*>(out_t + col * rows + row) =
                             make_uint4(o[kq][0], o[kq][1], o[kq][2], o[kq][3]);
+                    else
+                        *reinterpret_cast<uint2*>(out_t + col * rows + row) =
+                            make_uint2(o[kq][0], o[kq][1]);
                 }
             }
         }
@@ -244,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float* src = colsum + sb * kColsumFloats + tid;
                 float sum = src[0];
 #pragma unroll
-                for (int j = 1; j < 8; ++j) sum += src[j * kTileCols];
+                for (int j = 1; j < kWarps; ++j) sum += src[j * kTileCols];
                 p.partial[rt * cols + col0 + tid] = sum;
             }
         }
@@ -252,12 +359,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---- launch configuration ---------------------------------------------------
-constexpr int kStages = 4;
+// Pipeline depth: 4 stages while each CTA has few tiles (the prologue loads
+// dominate: keep as many in flight as possible), 3 stages for long runs
+// (measured on GB300: fewer outstanding tile loads per SM leave DRAM more
+// room for the output writes and sustain a higher read+write rate).
+// Resident CTAs per SM: 1 (compile-time constant).
+#ifndef CT_MINB
+#define CT_MINB 1
+#endif
+constexpr int kMinBlocks = CT_MINB;
+#ifndef CT_STAGES_SHORT
+#define CT_STAGES_SHORT 4
+#endif
+#ifndef CT_STAGES_LONG
+#define CT_STAGES_LONG 3
+#endif
+constexpr int kStagesShort = CT_STAGES_SHORT;
+constexpr int kStagesLong = CT_STAGES_LONG;
+constexpr int64_t kLongRunTiles = 16;   // tiles per CTA from which the long setting wins
 
 struct LaunchCache {
     std::mutex mu;
     int sms[64] = {0};
-    bool attr_done[64][16] = {};
+    bool attr_done[64][32] = {};
 };
 LaunchCache g_cache;
 
@@ -283,16 +407,36 @@ cudaError_t prepare(Kernel kernel, int key, int smem_bytes, int* sms_out) {
     return cudaSuccess;
 }
 
-template <int NT, int FMT, bool WRITE_T, bool DBIAS>
-cudaError_t launch_variant(const FastParams<NT>& p, int key, cudaStream_t stream) {
-    using L = SmemLayout<kStages, WRITE_T, DBIAS>;
-    auto kernel = fast_cast_transpose_kernel<NT, FMT, kStages, WRITE_T, DBIAS>;
+int device_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) {
+        std::lock_guard<std::mutex> lock(g_cache.mu);
+        if (g_cache.sms[dev]) return g_cache.sms[dev];
+    }
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms;
+}
+
+template <int NT, int FMT, int STAGES, bool WRITE_T, bool DBIAS>
+cudaError_t launch_stages(const FastParams<NT>& p, int key, cudaStream_t stream) {
+    using L = SmemLayout<STAGES, WRITE_T, DBIAS>;
+    auto kernel = fast_cast_transpose_kernel<NT, FMT, STAGES, kMinBlocks, WRITE_T, DBIAS>;
     int sms = 0;
     cudaError_t e = prepare(kernel, key, L::bytes, &sms);
     if (e != cudaSuccess) return e;
-    const int64_t grid = p.total_tiles < sms ? p.total_tiles : sms;
-    kernel<<<static_cast<unsigned>(grid), kThreads, L::bytes, stream>>>(p);
-    return cudaGetLastError();
+    const int64_t slots = int64_t(sms) * kMinBlocks;
+    const int64_t grid = p.total_tiles < slots ? p.total_tiles : slots;
+    return launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), dim3(kBlockThreads), L::bytes,
+                      stream, p);
+}
+
+template <int NT, int FMT, bool WRITE_T, bool DBIAS>
+cudaError_t launch_variant(const FastParams<NT>& p, int key, cudaStream_t stream) {
+    const int64_t slots = int64_t(device_sms()) * kMinBlocks;
+    if (slots > 0 && p.total_tiles > kLongRunTiles * slots)
+        return launch_stages<NT, FMT, kStagesLong, WRITE_T, DBIAS>(p, 2 * key + 1, stream);
+    return launch_stages<NT, FMT, kStagesShort, WRITE_T, DBIAS>(p, 2 * key, stream);
 }
 
 }  // namespace

@@ -24,6 +24,8 @@ constexpr int kGenCols = 32;
 
 template <int FMT, bool DBIAS>
 __global__ void __launch_bounds__(256) general_cast_kernel(GeneralArgs a) {
+    dev::pdl_launch_dependents();
+    dev::pdl_wait();
     if (a.noop != nullptr && *a.noop != 0.0f) return;
     __shared__ uint8_t tileq[kTileRows][kGenCols + 4];
     __shared__ float colsum[8][kGenCols];
@@ -87,30 +89,125 @@ __global__ void __launch_bounds__(256) general_cast_kernel(GeneralArgs a) {
 }
 
 // ---------------------------------------------------------------------------
+// db[j] = sum over row tiles t of partial[t, j], in fp64.  Block = 32 columns
+// x 8 row-tile groups; each thread sums every 8th tile of its column, then
+// the 8 group sums are added in a fixed order (deterministic).
 __global__ void __launch_bounds__(256) dbias_finish_kernel(const float* __restrict__ partial,
                                                            int64_t row_tiles, int64_t cols,
                                                            float* __restrict__ db,
                                                            const float* noop) {
+    dev::pdl_launch_dependents();
+    dev::pdl_wait();
     if (noop != nullptr && *noop != 0.0f) return;
-    for (int64_t j = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; j < cols;
-         j += int64_t(gridDim.x) * blockDim.x) {
+    __shared__ double part[8][32];
+    const int c = threadIdx.x & 31, g = threadIdx.x >> 5;
+    for (int64_t col0 = int64_t(blockIdx.x) * 32; col0 < cols; col0 += int64_t(gridDim.x) * 32) {
+        const int64_t j = col0 + c;
         double s = 0.0;
-        for (int64_t t = 0; t < row_tiles; ++t) s += static_cast<double>(partial[t * cols + j]);
-        db[j] = static_cast<float>(s);
+        if (j < cols) {
+#pragma unroll 4
+            for (int64_t t = g; t < row_tiles; t += 8) s += static_cast<double>(partial[t * cols + j]);
+        }
+        part[g][c] = s;
+        __syncthreads();
+        if (g == 0 && j < cols) {
+            double total = part[0][c];
+#pragma unroll
+            for (int k = 1; k < 8; ++k) total += part[k][c];
+            db[j] = static_cast<float>(total);
+        }
+        __syncthreads();
     }
 }
 
 // ---------------------------------------------------------------------------
-// Delayed scaling, one thread per tensor i:
-//   a = max over the L history rows (NaN propagates, the first NaN is kept),
+// Delayed scaling for tensor i:
+//   a = max over the L history rows (NaN propagates, the first NaN is kept;
+//       among equal values the earliest row is kept),
 //   s = (fp8_max / a) / 2^margin, kept only when a > 0, a finite, s finite,
 //   scale_inv = 1 / scale, then the window slides by one row.
-__global__ void __launch_bounds__(128) scale_update_kernel(float* __restrict__ hist,
-                                                           float* __restrict__ scale,
-                                                           float* __restrict__ scale_inv,
-                                                           int L, int n, float fp8_max,
-                                                           float two_pow_margin,
-                                                           const float* noop) {
+__device__ __forceinline__ void update_scale(float a, float fp8_max, float two_pow_margin,
+                                             float* scale, float* scale_inv, int i) {
+    float s = scale[i];
+    if (a > 0.0f && isfinite(a)) {
+        const float cand = __fdiv_rn(__fdiv_rn(fp8_max, a), two_pow_margin);
+        if (isfinite(cand)) s = cand;
+    }
+    scale[i] = s;
+    scale_inv[i] = __fdiv_rn(1.0f, s);
+}
+
+// (value, row) candidate order of the history maximum: a NaN beats any
+// number and an earlier NaN beats a later one; otherwise the larger value
+// wins and equal values go to the earlier row.  This is exactly the result
+// of scanning the rows in order, keeping the first NaN or a strictly larger
+// value, so any reduction tree gives the same bits.
+__device__ __forceinline__ bool better(float va, int ra, float vb, int rb) {
+    const bool na = isnan(va), nb = isnan(vb);
+    if (na || nb) return na && (!nb || ra < rb);
+    if (va != vb) return va > vb;
+    return ra < rb;
+}
+
+// One warp per tensor, for L <= 32 * kUpdateRowsPerLane: the column is read
+// once into registers (lane l holds rows l, l+32, ...), reduced with
+// shuffles, and written back shifted by one row; all reads precede all
+// writes, so the update costs one round trip to memory.
+constexpr int kUpdateRowsPerLane = 32;
+
+__global__ void __launch_bounds__(128) scale_update_warp_kernel(float* __restrict__ hist,
+                                                                float* __restrict__ scale,
+                                                                float* __restrict__ scale_inv,
+                                                                int L, int n, float fp8_max,
+                                                                float two_pow_margin,
+                                                                const float* noop) {
+    dev::pdl_launch_dependents();
+    dev::pdl_wait();
+    if (noop != nullptr && *noop != 0.0f) return;
+    const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (i >= n) return;
+    float v[kUpdateRowsPerLane];
+    float best = __int_as_float(0x7FFFFFFF);
+    int best_r = -1;
+#pragma unroll
+    for (int j = 0; j < kUpdateRowsPerLane; ++j) {
+        const int r = lane + 32 * j;
+        if (r < L) {
+            v[j] = hist[int64_t(r) * n + i];
+            if (best_r < 0 || better(v[j], r, best, best_r)) {
+                best = v[j];
+                best_r = r;
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xFFFFFFFFu, best, off);
+        const int orr = __shfl_xor_sync(0xFFFFFFFFu, best_r, off);
+        if (orr >= 0 && (best_r < 0 || better(ov, orr, best, best_r))) {
+            best = ov;
+            best_r = orr;
+        }
+    }
+    if (lane == 0) update_scale(best, fp8_max, two_pow_margin, scale, scale_inv, i);
+#pragma unroll
+    for (int j = 0; j < kUpdateRowsPerLane; ++j) {
+        const int r = lane + 32 * j;
+        if (r + 1 < L) hist[int64_t(r + 1) * n + i] = v[j];
+    }
+    if (lane == 0) hist[i] = 0.0f;
+}
+
+// Longer histories: one thread per tensor, sequential scan.
+__global__ void __launch_bounds__(128) scale_update_long_kernel(float* __restrict__ hist,
+                                                                float* __restrict__ scale,
+                                                                float* __restrict__ scale_inv,
+                                                                int L, int n, float fp8_max,
+                                                                float two_pow_margin,
+                                                                const float* noop) {
+    dev::pdl_launch_dependents();
+    dev::pdl_wait();
     if (noop != nullptr && *noop != 0.0f) return;
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
@@ -120,13 +217,7 @@ __global__ void __launch_bounds__(128) scale_update_kernel(float* __restrict__ h
         const float v = hist[int64_t(r) * n + i];
         if (isnan(v) || v > a) a = v;
     }
-    float s = scale[i];
-    if (a > 0.0f && isfinite(a)) {
-        const float cand = __fdiv_rn(__fdiv_rn(fp8_max, a), two_pow_margin);
-        if (isfinite(cand)) s = cand;
-    }
-    scale[i] = s;
-    scale_inv[i] = __fdiv_rn(1.0f, s);
+    update_scale(a, fp8_max, two_pow_margin, scale, scale_inv, i);
     for (int r = L - 1; r >= 1; --r) hist[int64_t(r) * n + i] = hist[int64_t(r - 1) * n + i];
     hist[i] = 0.0f;
 }
@@ -140,6 +231,8 @@ __global__ void __launch_bounds__(256) transpose_fast_kernel(const uint8_t* __re
                                                              int64_t rows, int64_t cols,
                                                              uint8_t* __restrict__ out,
                                                              const float* noop) {
+    dev::pdl_launch_dependents();
+    dev::pdl_wait();
     if (noop != nullptr && *noop != 0.0f) return;
     __shared__ __align__(16) uint32_t tile[kTileRows * (kTileCols / 4)];
     const int tid = threadIdx.x;
@@ -195,6 +288,8 @@ __global__ void __launch_bounds__(256) transpose_general_kernel(const uint8_t* _
                                                                 int64_t rows, int64_t cols,
                                                                 uint8_t* __restrict__ out,
                                                                 const float* noop) {
+    dev::pdl_launch_dependents();
+    dev::pdl_wait();
     if (noop != nullptr && *noop != 0.0f) return;
     __shared__ uint8_t tile[32][33];
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
@@ -226,23 +321,20 @@ unsigned grid_for(int64_t tiles, int64_t cap) {
 cudaError_t launch_general(const GeneralArgs& a, int fmt, cudaStream_t stream) {
     const int64_t tiles =
         ((a.rows + kTileRows - 1) / kTileRows) * ((a.cols + kGenCols - 1) / kGenCols);
-    const unsigned grid = grid_for(tiles, 1 << 20);
+    const dim3 grid(grid_for(tiles, 1 << 20)), block(256);
     const bool dbias = a.partial != nullptr;
-    if (fmt == 0) {
-        if (dbias) general_cast_kernel<0, true><<<grid, 256, 0, stream>>>(a);
-        else general_cast_kernel<0, false><<<grid, 256, 0, stream>>>(a);
-    } else {
-        if (dbias) general_cast_kernel<1, true><<<grid, 256, 0, stream>>>(a);
-        else general_cast_kernel<1, false><<<grid, 256, 0, stream>>>(a);
-    }
-    return cudaGetLastError();
+    if (fmt == 0)
+        return dbias ? launch_pdl(general_cast_kernel<0, true>, grid, block, 0, stream, a)
+                     : launch_pdl(general_cast_kernel<0, false>, grid, block, 0, stream, a);
+    return dbias ? launch_pdl(general_cast_kernel<1, true>, grid, block, 0, stream, a)
+                 : launch_pdl(general_cast_kernel<1, false>, grid, block, 0, stream, a);
 }
 
 cudaError_t launch_dbias_finish(const float* partial, int64_t row_tiles, int64_t cols,
                                 float* dbias, const float* noop, cudaStream_t stream) {
-    const unsigned grid = grid_for((cols + 255) / 256, 1 << 16);
-    dbias_finish_kernel<<<grid, 256, 0, stream>>>(partial, row_tiles, cols, dbias, noop);
-    return cudaGetLastError();
+    const dim3 grid(grid_for((cols + 31) / 32, 1 << 16)), block(256);
+    return launch_pdl(dbias_finish_kernel, grid, block, 0, stream, partial, row_tiles, cols, dbias,
+                      noop);
 }
 
 cudaError_t launch_scale_update(float* hist, float* scale, float* scale_inv, int hist_len,
@@ -250,24 +342,26 @@ cudaError_t launch_scale_update(float* hist, float* scale, float* scale_inv, int
                                 cudaStream_t stream) {
     const float fp8_max = fmt == 0 ? 448.0f : 57344.0f;
     const float two_pow_margin = std::ldexp(1.0f, margin);   // exact for 0 <= margin <= 126
-    const unsigned grid = static_cast<unsigned>((n + 127) / 128);
-    scale_update_kernel<<<grid, 128, 0, stream>>>(hist, scale, scale_inv, hist_len, n, fp8_max,
-                                                  two_pow_margin, noop);
-    return cudaGetLastError();
+    if (hist_len <= 32 * kUpdateRowsPerLane) {
+        const dim3 grid(static_cast<unsigned>((int64_t(n) * 32 + 127) / 128)), block(128);
+        return launch_pdl(scale_update_warp_kernel, grid, block, 0, stream, hist, scale, scale_inv,
+                          hist_len, n, fp8_max, two_pow_margin, noop);
+    }
+    const dim3 grid(static_cast<unsigned>((n + 127) / 128)), block(128);
+    return launch_pdl(scale_update_long_kernel, grid, block, 0, stream, hist, scale, scale_inv,
+                      hist_len, n, fp8_max, two_pow_margin, noop);
 }
 
 cudaError_t launch_transpose(const uint8_t* in, int64_t rows, int64_t cols, uint8_t* out,
                              const float* noop, bool fast, cudaStream_t stream) {
     if (fast) {
         const int64_t tiles = ((rows + 127) / 128) * ((cols + 127) / 128);
-        transpose_fast_kernel<<<grid_for(tiles, 4096), 256, 0, stream>>>(in, rows, cols, out,
-                                                                          noop);
-    } else {
-        const int64_t tiles = ((rows + 31) / 32) * ((cols + 31) / 32);
-        transpose_general_kernel<<<grid_for(tiles, 1 << 20), 256, 0, stream>>>(in, rows, cols,
-                                                                                out, noop);
+        return launch_pdl(transpose_fast_kernel, dim3(grid_for(tiles, 4096)), dim3(256), 0, stream,
+                          in, rows, cols, out, noop);
     }
-    return cudaGetLastError();
+    const int64_t tiles = ((rows + 31) / 32) * ((cols + 31) / 32);
+    return launch_pdl(transpose_general_kernel, dim3(grid_for(tiles, 1 << 20)), dim3(256), 0,
+                      stream, in, rows, cols, out, noop);
 }
 
 }  // namespace ct

@@ -31,6 +31,7 @@ struct FastTensor {
     int64_t tile_begin;    // first global tile index of this tensor
     int64_t tile_end;      // one past its last global tile index
     int64_t tile_cols;     // tiles per row of tiles
+    int64_t tile_rows;     // rows of tiles
 };
 
 template <int NT>
@@ -58,6 +59,26 @@ struct GeneralArgs {
 };
 
 enum class Fmt : int { E4M3 = 0, E5M2 = 1 };
+
+// Launch with programmatic stream serialisation allowed (see pdl_wait in
+// ct_device.cuh): the kernel may be scheduled while its predecessor in the
+// stream still runs, and waits for it on the device.  Recorded as a
+// programmatic edge when the stream is being captured into a graph.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
 
 // ---- launchers (return cudaGetLastError() of the launch) -----------------
 // TMA path.  `variant`: 0 = cast + transpose, 1 = cast only.  `dbias`
