@@ -213,6 +213,37 @@ int fp8_cast(const void* x, int64_t rows, int64_t cols, const float* scale,
              const float* noop_flag, void* stream);
 
 /*
+ * fp8_dbias_cast_transpose_noalloc -- fp8_dbias_cast_transpose without a
+ * caller-provided workspace.  The pages have no counterpart to this entry
+ * point: it exists for callers that cannot allocate device memory at the
+ * point of the call -- code running while a CUDA graph is captured (where
+ * cudaMalloc is not allowed), code called from inside an allocator or memory
+ * pool (where allocating again would recurse or deadlock), and runtimes that
+ * reserve all device memory up front.
+ *
+ *   dy, scale, amax, scale_inv, out, out_t, dbias, fmt, noop_flag, stream:
+ *              exactly as in fp8_dbias_cast_transpose
+ *
+ * Scratch: a fixed 4 MiB array inside the library's device memory (every
+ * GPU that loads the library holds it until the process exits).  The call
+ * itself allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library routine.  Limit: fp8_dbias_cast_transpose_workspace_size(rows,
+ * cols) <= 4 MiB, i.e. ceil(rows/128) * cols <= 1,048,576 (8192 x 16384,
+ * say); larger shapes return CT_ERR_WORKSPACE without launching anything.
+ * The first call on each device looks up the array's device address (once,
+ * with that device current), so make that first call before any stream
+ * capture.  All calls share the one array and nothing in it needs clearing,
+ * but calls whose kernels overlap on the GPU (different streams, or several
+ * threads) race on it: run them one after another.
+ * Errors: as fp8_dbias_cast_transpose, plus CT_ERR_WORKSPACE for too large
+ * a shape and CT_ERR_CUDA if the address lookup fails.
+ */
+int fp8_dbias_cast_transpose_noalloc(const void* dy, int64_t rows, int64_t cols,
+                                     const float* scale, float* amax, float* scale_inv,
+                                     void* out, void* out_t, float* dbias, int fmt,
+                                     const float* noop_flag, void* stream);
+
+/*
  * ct_device_error -- diagnostic word of the current device.  Kernels that
  * wait on an mbarrier give up after a bounded time (about two seconds)
  * instead of hanging, set a bit here and return early; in a correct run it
