@@ -118,7 +118,13 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
     // Rows of the staged tile loaded per batch in pass 1: all at once for the
     // most loads in flight, 4 when registers are tight.
     constexpr int kBatch = (DBIAS && (MINB > 1 || kFastThreads == 512)) ? 4 : 8 * 256 / kFastThreads;
-    dev::pdl_launch_dependents();
+    // When the next kernel of the stream may be scheduled.  Without dbias it
+    // is typically a one-warp scale update or the next cast, which either
+    // fits beside this kernel or cannot start before its CTAs leave: let it be
+    // scheduled right away, hiding its launch.  With dbias it is always the
+    // column-sum finish kernel, hundreds of blocks that would sit next to this
+    // kernel's for its whole run: schedule it from each CTA's last tile on.
+    if constexpr (!DBIAS) dev::pdl_launch_dependents();
 
     const uint32_t first = blockIdx.x;
     const uint32_t G = gridDim.x;
@@ -152,10 +158,6 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
         dev::fence_barrier_init();
     }
     __syncthreads();
-    // Everything above touched only shared memory and parameters; from here
-    // on global memory written by the preceding kernel may be read.
-    dev::pdl_wait();
-    if (p.noop != nullptr && *p.noop != 0.0f) return;
 
     // =============================== producer ================================
     if (warp == kWarps) {
@@ -163,12 +165,8 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
         const uint64_t policy = dev::policy_evict_first();
         int icur = 0;
         uint32_t issued = 0;
-        for (; issued < my_tiles; ++issued) {
-            const uint32_t kk = issued;
+        auto issue = [&](uint32_t kk) {
             const int s = static_cast<int>(kk % STAGES);
-            if (kk >= STAGES &&
-                !dev::mbar_wait_bounded(&empty[s], ((kk / STAGES) - 1) & 1u, s_abort))
-                break;
             const int64_t tile = int64_t(first) + int64_t(kk) * G;
             while (tile >= p.t[icur].tile_end) ++icur;
             const FastTensor& T = p.t[icur];
@@ -182,11 +180,23 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
             dev::mbar_arrive_expect_tx(&full[s], kStageBytes);
             dev::tma_load_2d(stages + s * kStageBytes, &p.map[icur], inf.ct * kTileCols,
                              inf.rt * kTileRows, &full[s], policy);
-        }
-        if (issued < my_tiles) {
-            // The consumers stopped (or never released a stage): flag it.
-            *s_abort = 1;
-            atomicOr(&g_device_error, kErrWaitTimeout);
+        };
+        // The first STAGES tile loads go out before the dependency wait: x is
+        // bf16 input, which no kernel of this library writes, so it can be
+        // fetched while the preceding kernel in the stream (when it is one of
+        // this library's, launched as a programmatic dependent) still runs.
+        for (; issued < my_tiles && issued < STAGES; ++issued) issue(issued);
+        dev::pdl_wait();
+        bool stop = p.noop != nullptr && *p.noop != 0.0f;
+        for (; !stop && issued < my_tiles; ++issued) {
+            const uint32_t kk = issued;
+            if (!dev::mbar_wait_bounded(&empty[kk % STAGES], ((kk / STAGES) - 1) & 1u, s_abort)) {
+                // The consumers stopped (or never released a stage): flag it.
+                *s_abort = 1;
+                atomicOr(&g_device_error, kErrWaitTimeout);
+                break;
+            }
+            issue(kk);
         }
         // Stay until the loads still in flight into this CTA's shared memory
         // have landed (bounded), whether or not the consumers still want them.
@@ -195,6 +205,11 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
             (void)dev::mbar_wait_bounded(&full[kk % STAGES], (kk / STAGES) & 1u);
         return;
     }
+
+    // Consumers read data the preceding kernel may have written (the noop
+    // flag, the scale, the amax slot): wait for it to complete first.
+    dev::pdl_wait();
+    if (p.noop != nullptr && *p.noop != 0.0f) return;
 
     // =============================== consumers ===============================
     int cur = -1;               // tensor of the current run, and its fields:
@@ -216,6 +231,7 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
     const int w = warp * (32 / kBlocks) + lane / kBlocks;
 
     for (uint32_t k = 0; k < my_tiles; ++k) {
+        if (DBIAS && k + 1 == my_tiles) dev::pdl_launch_dependents();
         const int s = static_cast<int>(k % STAGES);
         const int sb = static_cast<int>(k & 1u);
         uint8_t* sqb = sq + sb * kSqBytes;

@@ -126,9 +126,9 @@ __global__ void __launch_bounds__(256) dbias_finish_kernel(const float* __restri
 //       among equal values the earliest row is kept),
 //   s = (fp8_max / a) / 2^margin, kept only when a > 0, a finite, s finite,
 //   scale_inv = 1 / scale, then the window slides by one row.
-__device__ __forceinline__ void update_scale(float a, float fp8_max, float two_pow_margin,
-                                             float* scale, float* scale_inv, int i) {
-    float s = scale[i];
+__device__ __forceinline__ void update_scale(float a, float s, float fp8_max,
+                                             float two_pow_margin, float* scale,
+                                             float* scale_inv, int i) {
     if (a > 0.0f && isfinite(a)) {
         const float cand = __fdiv_rn(__fdiv_rn(fp8_max, a), two_pow_margin);
         if (isfinite(cand)) s = cand;
@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(128) scale_update_warp_kernel(float* __restric
     float v[kUpdateRowsPerLane];
     float best = __int_as_float(0x7FFFFFFF);
     int best_r = -1;
+    const float s_old = lane == 0 ? scale[i] : 0.0f;   // same round trip as the history
 #pragma unroll
     for (int j = 0; j < kUpdateRowsPerLane; ++j) {
         const int r = lane + 32 * j;
@@ -190,7 +191,7 @@ __global__ void __launch_bounds__(128) scale_update_warp_kernel(float* __restric
             best_r = orr;
         }
     }
-    if (lane == 0) update_scale(best, fp8_max, two_pow_margin, scale, scale_inv, i);
+    if (lane == 0) update_scale(best, s_old, fp8_max, two_pow_margin, scale, scale_inv, i);
 #pragma unroll
     for (int j = 0; j < kUpdateRowsPerLane; ++j) {
         const int r = lane + 32 * j;
@@ -217,7 +218,7 @@ __global__ void __launch_bounds__(128) scale_update_long_kernel(float* __restric
         const float v = hist[int64_t(r) * n + i];
         if (isnan(v) || v > a) a = v;
     }
-    update_scale(a, fp8_max, two_pow_margin, scale, scale_inv, i);
+    update_scale(a, scale[i], fp8_max, two_pow_margin, scale, scale_inv, i);
     for (int r = L - 1; r >= 1; --r) hist[int64_t(r) * n + i] = hist[int64_t(r - 1) * n + i];
     hist[i] = 0.0f;
 }

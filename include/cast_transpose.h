@@ -53,6 +53,13 @@
  *     the TMA-staged fast path, everything else a slower general kernel
  *     with identical results.
  *   - Calls are thread-safe; the library keeps no per-call state.
+ *   - Kernels are launched as programmatic dependents of the previous kernel
+ *     in the stream: a cast kernel may start fetching its bf16 input while
+ *     the library's preceding kernel on that stream is still finishing.
+ *     Every other read, and every write, waits for that kernel to complete.
+ *     The library never writes bf16 data, so this is invisible unless an
+ *     output buffer of the immediately preceding call is reinterpreted as
+ *     this call's bf16 input, which is not allowed.
  */
 #ifndef CAST_TRANSPOSE_GB300_H
 #define CAST_TRANSPOSE_GB300_H
