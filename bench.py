@@ -521,6 +521,35 @@ def extra_kernels(dev, peaks) -> dict:
     return res
 
 
+def profile_case(name: str) -> None:
+    """Three launches of one kernel on one workload, for a profiler to
+    capture (ncu -k ... -s 2 -c 1): 'activation' (cast-transpose of the
+    16384x12288 activation, E4M3) or 'gradient' (dbias cast-transpose of the
+    8192x12288 gradient, E5M2)."""
+    import torch
+
+    import cast_transpose_gb300 as ct
+    from cast_transpose_gb300 import workloads
+    dev = torch.device("cuda", 0)
+    s1, a0, si0 = (torch.tensor([v], dtype=torch.float32, device=dev) for v in (1.0, 0.0, 0.0))
+    if name == "activation":
+        x = workloads.activation_matrix(dev)
+        q, qt = ct.empty_outputs(x)
+        for _ in range(3):
+            ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3)
+    elif name == "gradient":
+        dy = workloads.gradient_matrix(dev)
+        q, qt = ct.empty_outputs(dy)
+        db = torch.empty(dy.shape[1], device=dev)
+        ws = torch.empty(ct.dbias_workspace_size(*dy.shape), dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            ct.fp8_dbias_cast_transpose(dy, s1, a0, si0, q, qt, db, ws, ct.E5M2)
+    else:
+        raise SystemExit(f"unknown profile case {name!r}")
+    torch.cuda.synchronize()
+    print(f"profile case {name}: 3 launches done")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -531,7 +560,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--extra", action=argparse.BooleanOptionalAction, default=True,
                     help="also time the dbias, multi-tensor and activation workloads")
+    ap.add_argument("--profile-case", choices=["activation", "gradient"], default=None,
+                    help="only run 3 launches of one workload's kernel (for ncu) and exit")
     args = ap.parse_args()
+    if args.profile_case:
+        profile_case(args.profile_case)
+        return
     if args.warmup < 3 and args.impl == "gb300":
         args.warmup = 3
     if args.impl == "reference":
