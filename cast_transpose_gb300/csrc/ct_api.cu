@@ -307,7 +307,7 @@ int fp8_amax_and_scale_update(float* amax_history, float* scale, float* scale_in
     const Range rh = range_of(amax_history, int64_t(4) * hist_len * n);
     const Range rs = range_of(scale, int64_t(4) * n), ri = range_of(scale_inv, int64_t(4) * n);
     if (overlap(rh, rs) || overlap(rh, ri) || overlap(rs, ri)) return CT_ERR_ALIAS;
-    return cuda_status(ct::launch_scale_update(amax_history, scale, scale_inv, hist_len, n, fmt,
+    return cuda_status(ct::launch_scale_update(amax_history, scale, scale_inv, hist_len, n, n, fmt,
                                                margin, noop_flag,
                                                static_cast<cudaStream_t>(stream)));
 }

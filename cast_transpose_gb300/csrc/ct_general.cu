@@ -11,6 +11,7 @@
 //     same page), a 128x128-tile vectorised one and a general one.
 #include "ct_device.cuh"
 #include "ct_internal.h"
+#include "ct_update.cuh"
 
 #include <cmath>
 
@@ -121,90 +122,29 @@ __global__ void __launch_bounds__(256) dbias_finish_kernel(const float* __restri
 }
 
 // ---------------------------------------------------------------------------
-// Delayed scaling for tensor i:
-//   a = max over the L history rows (NaN propagates, the first NaN is kept;
-//       among equal values the earliest row is kept),
-//   s = (fp8_max / a) / 2^margin, kept only when a > 0, a finite, s finite,
-//   scale_inv = 1 / scale, then the window slides by one row.
-__device__ __forceinline__ void update_scale(float a, float s, float fp8_max,
-                                             float two_pow_margin, float* scale,
-                                             float* scale_inv, int i) {
-    if (a > 0.0f && isfinite(a)) {
-        const float cand = __fdiv_rn(__fdiv_rn(fp8_max, a), two_pow_margin);
-        if (isfinite(cand)) s = cand;
-    }
-    scale[i] = s;
-    scale_inv[i] = __fdiv_rn(1.0f, s);
-}
-
-// (value, row) candidate order of the history maximum: a NaN beats any
-// number and an earlier NaN beats a later one; otherwise the larger value
-// wins and equal values go to the earlier row.  This is exactly the result
-// of scanning the rows in order, keeping the first NaN or a strictly larger
-// value, so any reduction tree gives the same bits.
-__device__ __forceinline__ bool better(float va, int ra, float vb, int rb) {
-    const bool na = isnan(va), nb = isnan(vb);
-    if (na || nb) return na && (!nb || ra < rb);
-    if (va != vb) return va > vb;
-    return ra < rb;
-}
-
-// One warp per tensor, for L <= 32 * kUpdateRowsPerLane: the column is read
-// once into registers (lane l holds rows l, l+32, ...), reduced with
-// shuffles, and written back shifted by one row; all reads precede all
-// writes, so the update costs one round trip to memory.
-constexpr int kUpdateRowsPerLane = 32;
-
+// Delayed scaling (rule in ct_update.cuh): one warp per tensor for histories
+// of up to 1024 rows, one thread per tensor beyond.
 __global__ void __launch_bounds__(128) scale_update_warp_kernel(float* __restrict__ hist,
                                                                 float* __restrict__ scale,
                                                                 float* __restrict__ scale_inv,
-                                                                int L, int n, float fp8_max,
+                                                                int L, int n, int64_t stride,
+                                                                float fp8_max,
                                                                 float two_pow_margin,
                                                                 const float* noop) {
     dev::pdl_launch_dependents();
     dev::pdl_wait();
     if (noop != nullptr && *noop != 0.0f) return;
     const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
     if (i >= n) return;
-    float v[kUpdateRowsPerLane];
-    float best = __int_as_float(0x7FFFFFFF);
-    int best_r = -1;
-    const float s_old = lane == 0 ? scale[i] : 0.0f;   // same round trip as the history
-#pragma unroll
-    for (int j = 0; j < kUpdateRowsPerLane; ++j) {
-        const int r = lane + 32 * j;
-        if (r < L) {
-            v[j] = hist[int64_t(r) * n + i];
-            if (best_r < 0 || better(v[j], r, best, best_r)) {
-                best = v[j];
-                best_r = r;
-            }
-        }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xFFFFFFFFu, best, off);
-        const int orr = __shfl_xor_sync(0xFFFFFFFFu, best_r, off);
-        if (orr >= 0 && (best_r < 0 || better(ov, orr, best, best_r))) {
-            best = ov;
-            best_r = orr;
-        }
-    }
-    if (lane == 0) update_scale(best, s_old, fp8_max, two_pow_margin, scale, scale_inv, i);
-#pragma unroll
-    for (int j = 0; j < kUpdateRowsPerLane; ++j) {
-        const int r = lane + 32 * j;
-        if (r + 1 < L) hist[int64_t(r + 1) * n + i] = v[j];
-    }
-    if (lane == 0) hist[i] = 0.0f;
+    dev::update_column_warp(hist + i, stride, L, scale + i, scale_inv + i, fp8_max, two_pow_margin,
+                            threadIdx.x & 31);
 }
 
-// Longer histories: one thread per tensor, sequential scan.
 __global__ void __launch_bounds__(128) scale_update_long_kernel(float* __restrict__ hist,
                                                                 float* __restrict__ scale,
                                                                 float* __restrict__ scale_inv,
-                                                                int L, int n, float fp8_max,
+                                                                int L, int n, int64_t stride,
+                                                                float fp8_max,
                                                                 float two_pow_margin,
                                                                 const float* noop) {
     dev::pdl_launch_dependents();
@@ -212,15 +152,8 @@ __global__ void __launch_bounds__(128) scale_update_long_kernel(float* __restric
     if (noop != nullptr && *noop != 0.0f) return;
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
-    float a = hist[i];
-    for (int r = 1; r < L; ++r) {
-        if (isnan(a)) break;
-        const float v = hist[int64_t(r) * n + i];
-        if (isnan(v) || v > a) a = v;
-    }
-    update_scale(a, scale[i], fp8_max, two_pow_margin, scale, scale_inv, i);
-    for (int r = L - 1; r >= 1; --r) hist[int64_t(r) * n + i] = hist[int64_t(r - 1) * n + i];
-    hist[i] = 0.0f;
+    dev::update_column_serial(hist + i, stride, L, scale + i, scale_inv + i, fp8_max,
+                              two_pow_margin);
 }
 
 // ---------------------------------------------------------------------------
@@ -339,18 +272,18 @@ cudaError_t launch_dbias_finish(const float* partial, int64_t row_tiles, int64_t
 }
 
 cudaError_t launch_scale_update(float* hist, float* scale, float* scale_inv, int hist_len,
-                                int n, int fmt, int margin, const float* noop,
-                                cudaStream_t stream) {
+                                int count, int64_t stride, int fmt, int margin,
+                                const float* noop, cudaStream_t stream) {
     const float fp8_max = fmt == 0 ? 448.0f : 57344.0f;
     const float two_pow_margin = std::ldexp(1.0f, margin);   // exact for 0 <= margin <= 126
-    if (hist_len <= 32 * kUpdateRowsPerLane) {
-        const dim3 grid(static_cast<unsigned>((int64_t(n) * 32 + 127) / 128)), block(128);
+    if (hist_len <= 32 * dev::kUpdateRowsPerLane) {
+        const dim3 grid(static_cast<unsigned>((int64_t(count) * 32 + 127) / 128)), block(128);
         return launch_pdl(scale_update_warp_kernel, grid, block, 0, stream, hist, scale, scale_inv,
-                          hist_len, n, fp8_max, two_pow_margin, noop);
+                          hist_len, count, stride, fp8_max, two_pow_margin, noop);
     }
-    const dim3 grid(static_cast<unsigned>((n + 127) / 128)), block(128);
+    const dim3 grid(static_cast<unsigned>((count + 127) / 128)), block(128);
     return launch_pdl(scale_update_long_kernel, grid, block, 0, stream, hist, scale, scale_inv,
-                      hist_len, n, fp8_max, two_pow_margin, noop);
+                      hist_len, count, stride, fp8_max, two_pow_margin, noop);
 }
 
 cudaError_t launch_transpose(const uint8_t* in, int64_t rows, int64_t cols, uint8_t* out,

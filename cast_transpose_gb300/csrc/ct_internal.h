@@ -95,10 +95,11 @@ cudaError_t launch_general(const GeneralArgs& a, int fmt, cudaStream_t stream);
 cudaError_t launch_dbias_finish(const float* partial, int64_t row_tiles, int64_t cols,
                                 float* dbias, const float* noop, cudaStream_t stream);
 
-// Scale update.
+// Scale update of `count` columns of a [hist_len, stride] history (scale and
+// scale_inv indexed like the columns).
 cudaError_t launch_scale_update(float* hist, float* scale, float* scale_inv, int hist_len,
-                                int n, int fmt, int margin, const float* noop,
-                                cudaStream_t stream);
+                                int count, int64_t stride, int fmt, int margin,
+                                const float* noop, cudaStream_t stream);
 
 // FP8 byte transpose.  `fast` requires rows % 16 == 0, cols % 16 == 0 and
 // 16-byte aligned pointers.
