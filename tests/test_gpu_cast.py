@@ -141,3 +141,32 @@ def test_weight_4096_eight_step_sequence(hist_init):
         assert np.array_equal(hist.cpu().numpy(), h_ref), f"step k={k}: history differs"
         assert f32_bits(scale.item()) == f32_bits(s_ref[0]), (k, scale.item(), s_ref[0])
         assert f32_bits(sinv.item()) == f32_bits(si_ref[0])
+
+
+def test_more_than_2_to_31_elements():
+    """49152 x 45056 = 2.2e9 elements: byte offsets of q and qT pass 2^31
+    (64-bit indexing).  Row blocks at the start, middle and end and the
+    transposed columns at the end are checked through the oracle; q^T == q
+    on the GPU for the whole matrix; amax against the oracle's full scan."""
+    rows, cols = 49152, 45056
+    g = torch.Generator(device="cuda").manual_seed(4242)
+    x = torch.empty(rows, cols, dtype=torch.bfloat16, device="cuda")
+    for r0 in range(0, rows, 8192):                  # generate in slabs (fp32 temp)
+        x[r0:r0 + 8192] = (torch.randn(8192, cols, generator=g, device="cuda") * 3.0).to(torch.bfloat16)
+    q, qt = ct.empty_outputs(x)
+    s, a, si = scalar(2.0), scalar(0.0), scalar(0.0)
+    ct.fp8_cast_transpose(x, s, a, si, q, qt, ct.E4M3)
+    torch.cuda.synchronize()
+    for r0 in (0, rows // 2 - 64, rows - 128):
+        xs = x[r0:r0 + 128].cpu()
+        ref = oracle.cast_transpose(xs, 2.0, ct.E4M3)
+        assert np.array_equal(q[r0:r0 + 128].cpu().numpy(), ref["q"]), r0
+        assert np.array_equal(qt[:, r0:r0 + 128].cpu().numpy(), ref["qt"]), r0
+    for c0 in (cols - 64,):
+        xs = x[:, c0:c0 + 64].contiguous().cpu()
+        ref = oracle.cast_transpose(xs, 2.0, ct.E4M3)
+        assert np.array_equal(qt[c0:c0 + 64].cpu().numpy(), ref["qt"])
+    for c0 in range(0, cols, 5632):                  # q^T == q, in column slabs
+        assert torch.equal(qt[c0:c0 + 5632], q[:, c0:c0 + 5632].t())
+    assert f32_bits(a.item()) == f32_bits(oracle.amax(x.cpu()))
+    assert si.item() == 0.5
