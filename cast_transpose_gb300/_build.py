@@ -72,7 +72,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         libdir = _cuda_lib_dir(nvcc)
         tmp = LIB + f".tmp{os.getpid()}"
         cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
-               "-Xlinker", f"-rpath,{libdir}"]
+               "-Xlinker", f"-rpath,{libdir}", "-Xlinker", "-z,defs"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             print(r.stdout + r.stderr)

@@ -124,9 +124,13 @@ void fill_tensor(FastTensor& t, const void* out, const void* out_t, const float*
     t.tile_end = tile_begin + t.tile_rows * t.tile_cols;
 }
 
+// `runs_out` (dbias only): the number of partial rows the launched kernel
+// writes per column (one per band of tile rows on the TMA path, one per tile
+// row on the general path).
 int cast_impl(const void* x, int64_t rows, int64_t cols, const float* scale, float* amax,
               float* scale_inv, void* out, void* out_t, float* partial, int fmt,
-              const float* noop, cudaStream_t stream) {
+              const float* noop, cudaStream_t stream, int64_t* runs_out = nullptr) {
+    const int64_t R = (rows + ct::kTileRows - 1) / ct::kTileRows;
     if (fast_eligible(x, rows, cols, out, out_t)) {
         FastParams<1> p;
         std::memset(&p, 0, sizeof(p));
@@ -136,6 +140,7 @@ int cast_impl(const void* x, int64_t rows, int64_t cols, const float* scale, flo
         p.total_tiles = p.t[0].tile_end;
         p.noop = noop;
         p.partial = partial;
+        if (runs_out) *runs_out = ct::dbias_units(R, R < ct::kDbiasBand ? R : ct::kDbiasBand).bands;
         return cuda_status(ct::launch_fast(p, fmt, partial != nullptr, out_t ? 0 : 1, stream));
     }
     ct::GeneralArgs a;
@@ -149,6 +154,7 @@ int cast_impl(const void* x, int64_t rows, int64_t cols, const float* scale, flo
     a.rows = rows;
     a.cols = cols;
     a.noop = noop;
+    if (runs_out) *runs_out = R;
     return cuda_status(ct::launch_general(a, fmt, stream));
 }
 
@@ -219,9 +225,11 @@ int fp8_dbias_cast_transpose(const void* dy, int64_t rows, int64_t cols, const f
         if (overlap(rdb, r) || overlap(rws, r)) return CT_ERR_ALIAS;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float* partial = static_cast<float*>(workspace);
-    st = cast_impl(dy, rows, cols, scale, amax, scale_inv, out, out_t, partial, fmt, noop_flag, s);
+    int64_t runs = 0;
+    st = cast_impl(dy, rows, cols, scale, amax, scale_inv, out, out_t, partial, fmt, noop_flag, s,
+                   &runs);
     if (st != CT_OK) return st;
-    return cuda_status(ct::launch_dbias_finish(partial, row_tiles(rows), cols, dbias, noop_flag, s));
+    return cuda_status(ct::launch_dbias_finish(partial, runs, cols, dbias, noop_flag, s));
 }
 
 int fp8_multi_cast_transpose(const ct_tensor_desc* descs, int n, int fmt,

@@ -72,7 +72,31 @@ struct StageInfo {
     int32_t last;          // 1: this CTA's last tile of that tensor
     int32_t rt;            // tile row
     int32_t ct;            // tile column
+    int32_t seg_end;       // dbias: 1 = last tile of this CTA's run down the strip
+    int32_t seg;           // dbias: partial-sum row of that run (see dbias_segment)
 };
+
+// Dbias tile schedule (dbias_units in ct_internal.h): CTA b takes units b,
+// b+G, ... and within a unit walks down its band's tile rows, summing the
+// columns over the band before writing one partial row.
+struct DbiasSchedule {
+    int64_t H, last_h, S, full_units;   // band height, last band height, strips, units of height H
+    int64_t F;                          // this CTA's units of height H
+    uint32_t tiles;                     // this CTA's tiles
+};
+__device__ __forceinline__ DbiasSchedule dbias_schedule(int64_t R, int64_t S, uint32_t b, uint32_t G) {
+    const DbiasUnits du = dbias_units(R, R < kDbiasBand ? R : kDbiasBand);
+    DbiasSchedule d;
+    d.H = du.H;
+    d.last_h = du.last_h;
+    d.S = S;
+    d.full_units = (du.bands - 1) * S;
+    const int64_t U = du.bands * S;
+    const int64_t M = b < U ? (U - b + G - 1) / G : 0;
+    d.F = b < d.full_units ? (d.full_units - b + G - 1) / G : 0;
+    d.tiles = static_cast<uint32_t>(d.F * d.H + (M - d.F) * d.last_h);
+    return d;
+}
 
 template <int STAGES, bool WRITE_T, bool DBIAS>
 struct SmemLayout {
@@ -129,7 +153,12 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
     const uint32_t first = blockIdx.x;
     const uint32_t G = gridDim.x;
     if (first >= p.total_tiles) return;
-    const uint32_t my_tiles = static_cast<uint32_t>((p.total_tiles - first + G - 1) / G);
+    // round-robin tiles (b, b+G, ...), or for dbias round-robin band units
+    DbiasSchedule dsch{};
+    if constexpr (DBIAS) dsch = dbias_schedule(p.t[0].tile_rows, p.t[0].tile_cols, first, G);
+    const uint32_t my_tiles =
+        DBIAS ? dsch.tiles : static_cast<uint32_t>((p.total_tiles - first + G - 1) / G);
+    if (my_tiles == 0) return;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -167,15 +196,39 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
         uint32_t issued = 0;
         auto issue = [&](uint32_t kk) {
             const int s = static_cast<int>(kk % STAGES);
-            const int64_t tile = int64_t(first) + int64_t(kk) * G;
-            while (tile >= p.t[icur].tile_end) ++icur;
-            const FastTensor& T = p.t[icur];
             StageInfo inf;
-            inf.tensor = icur;
-            inf.last = (kk + 1 == my_tiles) || (tile + G >= T.tile_end);
-            tile_coords(static_cast<uint32_t>(tile - T.tile_begin),
-                        static_cast<uint32_t>(T.tile_rows), static_cast<uint32_t>(T.tile_cols),
-                        inf.rt, inf.ct);
+            if constexpr (DBIAS) {
+                int64_t m, off, h;
+                if (int64_t(kk) < dsch.F * dsch.H) {
+                    m = kk / dsch.H;
+                    off = kk - m * dsch.H;
+                    h = dsch.H;
+                } else {
+                    const int64_t k2 = kk - dsch.F * dsch.H;
+                    m = dsch.F + k2 / dsch.last_h;
+                    off = k2 - (m - dsch.F) * dsch.last_h;
+                    h = dsch.last_h;
+                }
+                const int64_t u = int64_t(first) + m * G;
+                const int64_t band = u / dsch.S;
+                inf.tensor = 0;
+                inf.last = kk + 1 == my_tiles;
+                inf.ct = static_cast<int32_t>(u - band * dsch.S);
+                inf.rt = static_cast<int32_t>(band * dsch.H + off);
+                inf.seg_end = off + 1 == h;
+                inf.seg = static_cast<int32_t>(band);
+            } else {
+                const int64_t tile = int64_t(first) + int64_t(kk) * G;
+                while (tile >= p.t[icur].tile_end) ++icur;
+                const FastTensor& T = p.t[icur];
+                inf.tensor = icur;
+                inf.last = (kk + 1 == my_tiles) || (tile + G >= T.tile_end);
+                tile_coords(static_cast<uint32_t>(tile - T.tile_begin),
+                            static_cast<uint32_t>(T.tile_rows), static_cast<uint32_t>(T.tile_cols),
+                            inf.rt, inf.ct);
+                inf.seg_end = 0;
+                inf.seg = 0;
+            }
             info[s] = inf;
             dev::mbar_arrive_expect_tx(&full[s], kStageBytes);
             dev::tma_load_2d(stages + s * kStageBytes, &p.map[icur], inf.ct * kTileCols,
@@ -218,6 +271,9 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
     uint8_t* out = nullptr;
     uint8_t* out_t = nullptr;
     uint32_t amax_pair = 0;     // running bf16 magnitude max (pair form)
+    float cs[8];                // dbias: column sums of this thread's 8 columns over
+#pragma unroll                  // the current run down a strip
+    for (int j = 0; j < 8; ++j) cs[j] = 0.0f;
 
     // pass-1 mapping: column chunk c (8 columns), rows rg + kRowStep*it
     constexpr int kRowStep = kFastThreads / 16;           // 16 or 32
@@ -235,12 +291,9 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
         const int s = static_cast<int>(k % STAGES);
         const int sb = static_cast<int>(k & 1u);
         uint8_t* sqb = sq + sb * kSqBytes;
-        int64_t row0 = 0, col0 = 0, rt = 0;
-        bool last = false, first_tile = false;
-
-        float cs[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) cs[j] = 0.0f;
+        int64_t row0 = 0, col0 = 0;
+        int32_t seg = 0;
+        bool last = false, first_tile = false, seg_end = false;
 
         if (!dev::mbar_wait_bounded(&full[s], (k / STAGES) & 1u, s_abort)) {
             *s_abort = 1;
@@ -254,7 +307,8 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
                 out = p.t[cur].out;
                 out_t = p.t[cur].out_t;
             }
-            rt = inf.rt;
+            seg = inf.seg;
+            seg_end = inf.seg_end != 0;
             row0 = int64_t(inf.rt) * kTileRows;
             col0 = int64_t(inf.ct) * kTileCols;
             last = inf.last != 0;
@@ -299,13 +353,17 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
                 }
             }
             if constexpr (DBIAS) {
+                if (seg_end) {   // end of the run: fold the two row groups of the warp
 #pragma unroll
-                for (int j = 0; j < 8; ++j) cs[j] += __shfl_xor_sync(0xFFFFFFFFu, cs[j], 16);
-                if (lane < 16) {
-                    float4* dst = reinterpret_cast<float4*>(colsum + sb * kColsumFloats +
-                                                            warp * kTileCols + 8 * c);
-                    dst[0] = make_float4(cs[0], cs[1], cs[2], cs[3]);
-                    dst[1] = make_float4(cs[4], cs[5], cs[6], cs[7]);
+                    for (int j = 0; j < 8; ++j) cs[j] += __shfl_xor_sync(0xFFFFFFFFu, cs[j], 16);
+                    if (lane < 16) {
+                        float4* dst = reinterpret_cast<float4*>(colsum + sb * kColsumFloats +
+                                                                warp * kTileCols + 8 * c);
+                        dst[0] = make_float4(cs[0], cs[1], cs[2], cs[3]);
+                        dst[1] = make_float4(cs[4], cs[5], cs[6], cs[7]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) cs[j] = 0.0f;
                 }
             }
         }
@@ -363,12 +421,12 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
             }
         }
         if constexpr (DBIAS) {
-            if (tid < kTileCols && col0 + tid < cols) {
+            if (seg_end && tid < kTileCols && col0 + tid < cols) {
                 const float* src = colsum + sb * kColsumFloats + tid;
                 float sum = src[0];
 #pragma unroll
                 for (int j = 1; j < kWarps; ++j) sum += src[j * kTileCols];
-                p.partial[rt * cols + col0 + tid] = sum;
+                p.partial[int64_t(seg) * cols + col0 + tid] = sum;
             }
         }
     }

@@ -3,7 +3,7 @@
 //   * general_cast_kernel: cast (+ transpose, + dbias partials) of a bf16
 //     matrix of ANY shape and alignment, 128x32 tiles, element-wise loads;
 //   * dbias_finish_kernel: db[j] = sum over 128-row tiles of the partials,
-//     in fp64, in a fixed order (deterministic);
+//     compensated fp32, in a fixed order (deterministic);
 //   * scale_update_kernel: the delayed-scaling update of "[PyTorch] Refactor
 //     FP8 workspaces in linear modules" (Motivations: scale update kernel,
 //     infinite-scale case), one thread per tensor;
@@ -90,32 +90,51 @@ __global__ void __launch_bounds__(256) general_cast_kernel(GeneralArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// db[j] = sum over row tiles t of partial[t, j], in fp64.  Block = 32 columns
-// x 8 row-tile groups; each thread sums every 8th tile of its column, then
-// the 8 group sums are added in a fixed order (deterministic).
+// db[j] = sum over the `runs` partial rows of partial[t, j] (one row per
+// band of tile rows, see dbias_units).  Block = 32 columns x 8 row groups;
+// each thread sums every 8th partial row of its column, then the 8 group
+// sums are added in a fixed order (deterministic).  The sums are
+// compensated (Kahan) fp32: the error stays within a few fp32 ulps of the sum
+// of magnitudes for any number of row tiles, without fp64 arithmetic, which
+// runs at a small fraction of the fp32 rate on this GPU.
+struct Kahan {
+    float sum = 0.0f, comp = 0.0f;
+    __device__ __forceinline__ void add(float v) {
+        const float y = __fsub_rn(v, comp);
+        const float t = __fadd_rn(sum, y);
+        comp = __fsub_rn(__fsub_rn(t, sum), y);
+        sum = t;
+    }
+};
+
 __global__ void __launch_bounds__(256) dbias_finish_kernel(const float* __restrict__ partial,
-                                                           int64_t row_tiles, int64_t cols,
+                                                           int64_t runs, int64_t cols,
                                                            float* __restrict__ db,
                                                            const float* noop) {
     dev::pdl_launch_dependents();
     dev::pdl_wait();
     if (noop != nullptr && *noop != 0.0f) return;
-    __shared__ double part[8][32];
+    __shared__ float part[8][32];
+    __shared__ float comp[8][32];
     const int c = threadIdx.x & 31, g = threadIdx.x >> 5;
     for (int64_t col0 = int64_t(blockIdx.x) * 32; col0 < cols; col0 += int64_t(gridDim.x) * 32) {
         const int64_t j = col0 + c;
-        double s = 0.0;
+        Kahan k;
         if (j < cols) {
 #pragma unroll 4
-            for (int64_t t = g; t < row_tiles; t += 8) s += static_cast<double>(partial[t * cols + j]);
+            for (int64_t t = g; t < runs; t += 8) k.add(partial[t * cols + j]);
         }
-        part[g][c] = s;
+        part[g][c] = k.sum;
+        comp[g][c] = k.comp;
         __syncthreads();
         if (g == 0 && j < cols) {
-            double total = part[0][c];
+            Kahan total;
 #pragma unroll
-            for (int k = 1; k < 8; ++k) total += part[k][c];
-            db[j] = static_cast<float>(total);
+            for (int q = 0; q < 8; ++q) {
+                total.add(part[q][c]);
+                total.add(-comp[q][c]);
+            }
+            db[j] = total.sum;
         }
         __syncthreads();
     }
@@ -264,11 +283,10 @@ cudaError_t launch_general(const GeneralArgs& a, int fmt, cudaStream_t stream) {
                  : launch_pdl(general_cast_kernel<1, false>, grid, block, 0, stream, a);
 }
 
-cudaError_t launch_dbias_finish(const float* partial, int64_t row_tiles, int64_t cols,
-                                float* dbias, const float* noop, cudaStream_t stream) {
+cudaError_t launch_dbias_finish(const float* partial, int64_t runs, int64_t cols, float* dbias,
+                                const float* noop, cudaStream_t stream) {
     const dim3 grid(grid_for((cols + 31) / 32, 1 << 16)), block(256);
-    return launch_pdl(dbias_finish_kernel, grid, block, 0, stream, partial, row_tiles, cols, dbias,
-                      noop);
+    return launch_pdl(dbias_finish_kernel, grid, block, 0, stream, partial, runs, cols, dbias, noop);
 }
 
 cudaError_t launch_scale_update(float* hist, float* scale, float* scale_inv, int hist_len,

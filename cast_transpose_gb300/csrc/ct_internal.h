@@ -91,9 +91,36 @@ cudaError_t launch_fast_list(const FastParams<kMaxListPerLaunch>& p, int fmt,
 // General path.
 cudaError_t launch_general(const GeneralArgs& a, int fmt, cudaStream_t stream);
 
-// Dbias finish: db[j] = sum over row tiles of partial[rt, j] (fp64 sum).
-cudaError_t launch_dbias_finish(const float* partial, int64_t row_tiles, int64_t cols,
-                                float* dbias, const float* noop, cudaStream_t stream);
+// Dbias schedule and partial sums.  The TMA kernel splits the R = ceil(rows
+// / 128) tile rows into bands of H = min(kDbiasBand, R) tile rows (the last
+// band may be shorter) and hands out "units" -- one band of one 128-column strip,
+// unit u = band * S + strip -- round-robin to its CTAs.  A CTA walks down
+// the H tiles of a unit, sums its columns over them, and writes one partial
+// row per band: partial[band][col].  CTAs running at the same time work on
+// neighbouring strips of the same band, i.e. on the same rows of x.  The
+// general kernel writes one partial row per tile row, i.e. H = 1.
+struct DbiasUnits {
+    int64_t H;        // tile rows per full band
+    int64_t bands;    // ceil(R / H)
+    int64_t last_h;   // tile rows of the last band
+};
+__host__ __device__ __forceinline__ DbiasUnits dbias_units(int64_t R, int64_t H) {
+    DbiasUnits u;
+    u.H = H;
+    u.bands = (R + H - 1) / H;
+    u.last_h = R - (u.bands - 1) * H;
+    return u;
+}
+// Band height: 4 measured best on GB300 (shorter bands balance the last
+// wave of units better, longer ones write fewer partial rows).
+#ifndef CT_DBIAS_BAND
+#define CT_DBIAS_BAND 4
+#endif
+constexpr int64_t kDbiasBand = CT_DBIAS_BAND;
+
+// Dbias finish: db[j] = sum of the `runs` partial rows (compensated fp32).
+cudaError_t launch_dbias_finish(const float* partial, int64_t runs, int64_t cols, float* dbias,
+                                const float* noop, cudaStream_t stream);
 
 // Scale update of `count` columns of a [hist_len, stride] history (scale and
 // scale_inv indexed like the columns).

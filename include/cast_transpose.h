@@ -120,8 +120,9 @@ int fp8_cast_transpose(const void* x, int64_t rows, int64_t cols,
  *   dy, scale, amax, scale_inv, out, out_t, fmt, noop_flag: as in
  *              fp8_cast_transpose, with dy in place of x
  *   dbias      fp32 [cols] output: column sums of the unscaled dy,
- *              accumulated in fp32 per 128-row tile and in fp64 across tiles;
- *              deterministic (the summation order depends only on the shape)
+ *              accumulated in fp32 per 128-row tile and with compensated
+ *              (Kahan) fp32 across tiles; deterministic (the summation order
+ *              depends only on the shape)
  *   workspace  device scratch of at least
  *              fp8_dbias_cast_transpose_workspace_size(rows, cols) bytes,
  *              16-byte aligned; its contents on entry are ignored and on exit

@@ -54,7 +54,7 @@ def check(got, x_cpu, scale, fmt, amax_in=0.0):
 
 
 SHAPES = [(1, 1), (3, 17), (128, 128), (127, 129), (129, 256), (1000, 48), (2048, 272),
-          (4112, 1040)]
+          (4112, 1040), (131072, 256), (131000, 33)]
 
 
 @pytest.mark.parametrize("fmt", [ct.E4M3, ct.E5M2])
