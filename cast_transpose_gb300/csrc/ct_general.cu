@@ -48,13 +48,22 @@ __global__ void __launch_bounds__(256) general_cast_kernel(GeneralArgs a) {
         const int64_t col0 = (tile - rt * tiles_c) * kGenCols;
         const int64_t col = col0 + c;
         float cs = 0.0f;
-#pragma unroll 4
+        // all 16 loads of the thread first (memory-level parallelism), then
+        // the conversions and stores
+        uint16_t xv[16];
+        const bool col_ok = col < a.cols;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int64_t row = row0 + g + 8 * i;
+            xv[i] = (col_ok && row < a.rows) ? __ldg(a.x + row * a.cols + col) : uint16_t(0);
+        }
+#pragma unroll
         for (int i = 0; i < 16; ++i) {
             const int r = g + 8 * i;
             const int64_t row = row0 + r;
             uint8_t code = 0;
-            if (row < a.rows && col < a.cols) {
-                const uint32_t bits = a.x[row * a.cols + col];
+            if (col_ok && row < a.rows) {
+                const uint32_t bits = xv[i];
                 const uint32_t mag = (bits & 0x7FFFu) << 16;
                 amax = mag > amax ? mag : amax;
                 const float f = __uint_as_float(bits << 16);
@@ -251,10 +260,14 @@ __global__ void __launch_bounds__(256) transpose_general_kernel(const uint8_t* _
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
         const int64_t rt = t / tiles_c;
         const int64_t row0 = rt * 32, col0 = (t - rt * tiles_c) * 32;
-        for (int r = ty; r < 32; r += 8) {
-            const int64_t row = row0 + r, col = col0 + tx;
-            if (row < rows && col < cols) tile[r][tx] = in[row * cols + col];
+        uint8_t v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t row = row0 + ty + 8 * i, col = col0 + tx;
+            v[i] = (row < rows && col < cols) ? __ldg(in + row * cols + col) : uint8_t(0);
         }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tile[ty + 8 * i][tx] = v[i];
         __syncthreads();
         for (int cc = ty; cc < 32; cc += 8) {
             const int64_t col = col0 + cc, row = row0 + tx;
