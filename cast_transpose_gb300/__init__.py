@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
             L.fp8_amax_and_scale_update.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp]
             L.fp8_transpose.argtypes = [vp, i64, i64, vp, vp, vp]
             L.ct_device_error.argtypes = [c.POINTER(c.c_uint), i32]
+            L.ct_selftest_bounded_wait.argtypes = [c.c_uint, vp]
+            L.ct_selftest_bounded_wait.restype = i32
             for name in ("fp8_cast_transpose", "fp8_cast", "fp8_dbias_cast_transpose",
                          "fp8_multi_cast_transpose", "fp8_amax_and_scale_update",
                          "fp8_transpose", "ct_device_error"):
@@ -209,6 +211,12 @@ def device_error(clear: bool = False) -> int:
     v = ctypes.c_uint(0)
     _check(lib().ct_device_error(ctypes.byref(v), 1 if clear else 0))
     return v.value
+
+
+def selftest_bounded_wait(limit_us: int = 20000, stream=None) -> None:
+    """Launch the bounded-wait self-test (its wait times out by design and
+    sets bit 2 of the device diagnostic word)."""
+    _check(lib().ct_selftest_bounded_wait(limit_us, _stream(stream)))
 
 
 def empty_outputs(x: torch.Tensor):

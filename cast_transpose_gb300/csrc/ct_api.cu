@@ -332,6 +332,11 @@ int fp8_transpose(const void* in, int64_t rows, int64_t cols, void* out, const f
                                             static_cast<cudaStream_t>(stream)));
 }
 
+int ct_selftest_bounded_wait(unsigned int limit_us, void* stream) {
+    if (limit_us == 0 || limit_us > 1000000u) return CT_ERR_ARG;
+    return cuda_status(ct::launch_wait_selftest(limit_us, static_cast<cudaStream_t>(stream)));
+}
+
 int ct_device_error(unsigned int* value_out, int clear) {
     if (!value_out) return CT_ERR_NULL;
     return cuda_status(ct::read_device_error(value_out, clear != 0));

@@ -539,6 +539,24 @@ cudaError_t launch_fast_list(const FastParams<kMaxListPerLaunch>& p, int fmt,
                     : launch_variant<kMaxListPerLaunch, 1, true, false>(p, 7, stream);
 }
 
+namespace {
+// The mbarrier expects one arrival that never comes: the wait must give up
+// after limit_ns, leave a mark in the diagnostic word and return, exactly as
+// the tile-load waits of the cast kernels do.
+__global__ void wait_selftest_kernel(uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    dev::mbar_init(&bar, 1);
+    dev::fence_barrier_init();
+    if (!dev::mbar_wait_bounded(&bar, 0, limit_ns)) atomicOr(&g_device_error, kErrSelftestTimeout);
+}
+}  // namespace
+
+cudaError_t launch_wait_selftest(uint32_t limit_us, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(uint64_t(limit_us) * 1000ull);
+    return cudaGetLastError();
+}
+
 cudaError_t read_device_error(unsigned* value, bool clear) {
     cudaError_t e = cudaMemcpyFromSymbol(value, g_device_error, sizeof(unsigned));
     if (e != cudaSuccess || !clear) return e;

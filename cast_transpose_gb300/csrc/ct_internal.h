@@ -16,8 +16,9 @@ constexpr int kTileCols = 128;
 constexpr int kThreads = 256;
 constexpr int kMaxListPerLaunch = 64;
 
-// Bit set in the device diagnostic word when an mbarrier wait gave up.
-constexpr unsigned kErrWaitTimeout = 1u;
+// Bits of the device diagnostic word.
+constexpr unsigned kErrWaitTimeout = 1u;      // a kernel's mbarrier wait gave up
+constexpr unsigned kErrSelftestTimeout = 2u;  // the bounded-wait self-test gave up (expected)
 
 // One tensor of a TMA-path launch.  Pointers are device pointers.
 struct FastTensor {
@@ -135,6 +136,10 @@ cudaError_t launch_transpose(const uint8_t* in, int64_t rows, int64_t cols, uint
 
 // Diagnostic word (device of the calling thread).
 cudaError_t read_device_error(unsigned* value, bool clear);
+
+// Bounded-wait self-test: one CTA waits `limit_us` on an mbarrier that
+// nothing completes, then records kErrSelftestTimeout and returns.
+cudaError_t launch_wait_selftest(uint32_t limit_us, cudaStream_t stream);
 
 // Number of SMs and persistent CTAs per SM for the TMA kernels of this
 // device (cached per device).

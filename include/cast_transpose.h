@@ -256,9 +256,19 @@ int fp8_dbias_cast_transpose_noalloc(const void* dy, int64_t rows, int64_t cols,
  * wait on an mbarrier give up after a bounded time (about two seconds)
  * instead of hanging, set a bit here and return early; in a correct run it
  * stays 0.  Reads (synchronously) and optionally clears the word.
- * Bits: 1 = a tile-load wait timed out.
+ * Bits: 1 = a tile-load wait timed out; 2 = ct_selftest_bounded_wait ran
+ * (its wait always times out).
  */
 int ct_device_error(unsigned int* value_out, int clear);
+
+/*
+ * ct_selftest_bounded_wait -- exercises the timeout path of the kernels'
+ * bounded waits without any fault: one block waits `limit_us` microseconds
+ * (1 .. 1,000,000) on a barrier that nothing completes, then sets bit 2 of
+ * the diagnostic word and returns; the context stays usable.  For tests and
+ * health checks.  Errors: CT_ERR_ARG, CT_ERR_CUDA.
+ */
+int ct_selftest_bounded_wait(unsigned int limit_us, void* stream);
 
 #ifdef __cplusplus
 }

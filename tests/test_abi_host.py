@@ -148,3 +148,8 @@ def test_python_binding_rejects_cpu_tensors():
     with pytest.raises(ValueError):
         ct.fp8_cast_transpose(x, torch.ones(1), torch.zeros(1), torch.zeros(1),
                               torch.empty(16, dtype=torch.uint8), torch.empty(16, dtype=torch.uint8))
+
+
+def test_selftest_rejects_bad_limits(L):
+    assert L.ct_selftest_bounded_wait(0, None) == CT_ERR_ARG
+    assert L.ct_selftest_bounded_wait(2000000, None) == CT_ERR_ARG
