@@ -76,13 +76,17 @@ def lib() -> ctypes.CDLL:
             L.fp8_dbias_cast_transpose_workspace_size.restype = c.c_size_t
             L.fp8_dbias_cast_transpose_workspace_size.argtypes = [i64, i64]
             L.fp8_multi_cast_transpose.argtypes = [vp, i32, i32, vp, vp]
+            L.fp8_multi_cast_transpose_ex.argtypes = [vp, vp, i32, vp, vp]
             L.fp8_amax_and_scale_update.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp]
+            L.fp8_amax_and_scale_update_ex.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp,
+                                                       vp]
             L.fp8_transpose.argtypes = [vp, i64, i64, vp, vp, vp]
             L.ct_device_error.argtypes = [c.POINTER(c.c_uint), i32]
             L.ct_selftest_bounded_wait.argtypes = [c.c_uint, vp]
             L.ct_selftest_bounded_wait.restype = i32
             for name in ("fp8_cast_transpose", "fp8_cast", "fp8_dbias_cast_transpose",
-                         "fp8_multi_cast_transpose", "fp8_amax_and_scale_update",
+                         "fp8_multi_cast_transpose", "fp8_multi_cast_transpose_ex",
+                         "fp8_amax_and_scale_update", "fp8_amax_and_scale_update_ex",
                          "fp8_transpose", "ct_device_error"):
                 getattr(L, name).restype = i32
             _lib = L
@@ -170,10 +174,7 @@ def fp8_dbias_cast_transpose(dy, scale, amax, scale_inv, out, out_t, dbias, work
         _opt(noop_flag, "noop_flag"), _stream(stream)))
 
 
-def fp8_multi_cast_transpose(xs, scales, amaxes, scale_invs, outs, outs_t, fmt=E4M3,
-                             noop_flag=None, stream=None) -> None:
-    """Each of scales/amaxes/scale_invs is a list of 1-element fp32 tensors
-    (views into one buffer are fine)."""
+def _descs(xs, scales, amaxes, scale_invs, outs, outs_t):
     n = len(xs)
     if not (len(scales) == len(amaxes) == len(scale_invs) == len(outs) == len(outs_t) == n):
         raise ValueError("all lists must have the same length")
@@ -186,8 +187,27 @@ def fp8_multi_cast_transpose(xs, scales, amaxes, scale_invs, outs, outs_t, fmt=E
                          _dev(amaxes[i], f"amaxes[{i}]", torch.float32, 1),
                          _dev(scale_invs[i], f"scale_invs[{i}]", torch.float32, 1),
                          _dev(outs[i], f"outs[{i}]", _U8, m), _dev(outs_t[i], f"outs_t[{i}]", _U8, m))
+    return descs, n
+
+
+def fp8_multi_cast_transpose(xs, scales, amaxes, scale_invs, outs, outs_t, fmt=E4M3,
+                             noop_flag=None, stream=None) -> None:
+    """Each of scales/amaxes/scale_invs is a list of 1-element fp32 tensors
+    (views into one buffer are fine)."""
+    descs, n = _descs(xs, scales, amaxes, scale_invs, outs, outs_t)
     _check(lib().fp8_multi_cast_transpose(descs, n, fmt, _opt(noop_flag, "noop_flag"),
                                           _stream(stream)))
+
+
+def fp8_multi_cast_transpose_ex(xs, scales, amaxes, scale_invs, outs, outs_t, fmts,
+                                noop_flag=None, stream=None) -> None:
+    """As fp8_multi_cast_transpose with one FP8 format per tensor."""
+    descs, n = _descs(xs, scales, amaxes, scale_invs, outs, outs_t)
+    if len(fmts) != n:
+        raise ValueError("one format per tensor")
+    fmt_arr = (ctypes.c_int * max(n, 1))(*fmts)
+    _check(lib().fp8_multi_cast_transpose_ex(descs, fmt_arr, n, _opt(noop_flag, "noop_flag"),
+                                             _stream(stream)))
 
 
 def fp8_amax_and_scale_update(amax_history, scale, scale_inv, fmt=E4M3, margin=0,
@@ -198,6 +218,21 @@ def fp8_amax_and_scale_update(amax_history, scale, scale_inv, fmt=E4M3, margin=0
     _check(lib().fp8_amax_and_scale_update(
         _dev(amax_history, "amax_history", torch.float32), _dev(scale, "scale", torch.float32, n),
         _dev(scale_inv, "scale_inv", torch.float32, n), L, n, fmt, margin,
+        _opt(noop_flag, "noop_flag"), _stream(stream)))
+
+
+AMAX_MAX = 0
+AMAX_MOST_RECENT = 1
+
+
+def fp8_amax_and_scale_update_ex(amax_history, scale, scale_inv, fmt=E4M3, margin=0,
+                                 amax_algo=AMAX_MAX, noop_flag=None, stream=None) -> None:
+    if amax_history.dim() != 2:
+        raise ValueError("amax_history must be [hist_len, n]")
+    L, n = amax_history.shape
+    _check(lib().fp8_amax_and_scale_update_ex(
+        _dev(amax_history, "amax_history", torch.float32), _dev(scale, "scale", torch.float32, n),
+        _dev(scale_inv, "scale_inv", torch.float32, n), L, n, fmt, margin, amax_algo,
         _opt(noop_flag, "noop_flag"), _stream(stream)))
 
 

@@ -232,16 +232,20 @@ int fp8_dbias_cast_transpose(const void* dy, int64_t rows, int64_t cols, const f
     return cuda_status(ct::launch_dbias_finish(partial, runs, cols, dbias, noop_flag, s));
 }
 
-int fp8_multi_cast_transpose(const ct_tensor_desc* descs, int n, int fmt,
-                             const float* noop_flag, void* stream) {
+namespace {
+// Shared by the single-format and per-tensor-format list entry points:
+// fmts == nullptr means every entry uses `fmt`.
+int multi_impl(const ct_tensor_desc* descs, const int* fmts, int n, int fmt,
+               const float* noop_flag, cudaStream_t s) {
     if (n < 0) return CT_ERR_ARG;
     if (n == 0) return CT_OK;
     if (!descs) return CT_ERR_NULL;
-    if (fmt != CT_E4M3 && fmt != CT_E5M2) return CT_ERR_FORMAT;
+    auto fmt_of = [&](int i) { return fmts ? fmts[i] : fmt; };
+    if (!fmts && fmt != CT_E4M3 && fmt != CT_E5M2) return CT_ERR_FORMAT;
     for (int i = 0; i < n; ++i) {
         const ct_tensor_desc& d = descs[i];
         const int st = check_cast(d.x, d.rows, d.cols, d.scale, d.amax, d.scale_inv, d.out,
-                                  d.out_t, true, fmt);
+                                  d.out_t, true, fmt_of(i));
         if (st != CT_OK) return st;
     }
     // outputs of one entry must not overlap anything of another entry
@@ -263,7 +267,6 @@ int fp8_multi_cast_transpose(const ct_tensor_desc* descs, int n, int fmt,
                     if (overlap(r1, r2)) return CT_ERR_ALIAS;
         }
     }
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     // fast entries go into list launches of up to kMaxListPerLaunch tensors
     std::vector<int> fast, general;
     for (int i = 0; i < n; ++i) {
@@ -280,6 +283,7 @@ int fp8_multi_cast_transpose(const ct_tensor_desc* descs, int n, int fmt,
             const ct_tensor_desc& d = descs[fast[k]];
             if (!encode_bf16_map(&p.map[m], d.x, d.rows, d.cols)) return CT_ERR_CUDA;
             fill_tensor(p.t[m], d.out, d.out_t, d.scale, d.amax, d.scale_inv, d.rows, d.cols, tiles);
+            p.t[m].fmt = fmt_of(fast[k]);
             tiles = p.t[m].tile_end;
         }
         // unused slots: empty tile ranges past the end
@@ -291,22 +295,35 @@ int fp8_multi_cast_transpose(const ct_tensor_desc* descs, int n, int fmt,
         p.total_tiles = tiles;
         p.noop = noop_flag;
         p.partial = nullptr;
-        const int st = cuda_status(ct::launch_fast_list(p, fmt, s));
+        const int st = cuda_status(ct::launch_fast_list(p, fmts ? -1 : fmt, s));
         if (st != CT_OK) return st;
     }
     for (int i : general) {
         const ct_tensor_desc& d = descs[i];
         const int st = cast_impl(d.x, d.rows, d.cols, d.scale, d.amax, d.scale_inv, d.out, d.out_t,
-                                 nullptr, fmt, noop_flag, s);
+                                 nullptr, fmt_of(i), noop_flag, s);
         if (st != CT_OK) return st;
     }
     return CT_OK;
 }
+}  // namespace
 
-int fp8_amax_and_scale_update(float* amax_history, float* scale, float* scale_inv,
-                              int hist_len, int n, int fmt, int margin,
-                              const float* noop_flag, void* stream) {
+int fp8_multi_cast_transpose(const ct_tensor_desc* descs, int n, int fmt,
+                             const float* noop_flag, void* stream) {
+    return multi_impl(descs, nullptr, n, fmt, noop_flag, static_cast<cudaStream_t>(stream));
+}
+
+int fp8_multi_cast_transpose_ex(const ct_tensor_desc* descs, const int* fmts, int n,
+                                const float* noop_flag, void* stream) {
+    if (n > 0 && !fmts) return CT_ERR_NULL;
+    return multi_impl(descs, fmts, n, CT_E4M3, noop_flag, static_cast<cudaStream_t>(stream));
+}
+
+int fp8_amax_and_scale_update_ex(float* amax_history, float* scale, float* scale_inv,
+                                 int hist_len, int n, int fmt, int margin, int amax_algo,
+                                 const float* noop_flag, void* stream) {
     if (n < 0 || hist_len < 1 || margin < 0 || margin > 126) return CT_ERR_ARG;
+    if (amax_algo != CT_AMAX_MAX && amax_algo != CT_AMAX_MOST_RECENT) return CT_ERR_ARG;
     if (fmt != CT_E4M3 && fmt != CT_E5M2) return CT_ERR_FORMAT;
     if (n == 0) return CT_OK;
     if (!amax_history || !scale || !scale_inv) return CT_ERR_NULL;
@@ -316,8 +333,15 @@ int fp8_amax_and_scale_update(float* amax_history, float* scale, float* scale_in
     const Range rs = range_of(scale, int64_t(4) * n), ri = range_of(scale_inv, int64_t(4) * n);
     if (overlap(rh, rs) || overlap(rh, ri) || overlap(rs, ri)) return CT_ERR_ALIAS;
     return cuda_status(ct::launch_scale_update(amax_history, scale, scale_inv, hist_len, n, n, fmt,
-                                               margin, noop_flag,
-                                               static_cast<cudaStream_t>(stream)));
+                                               margin, amax_algo == CT_AMAX_MOST_RECENT ? 1 : 0,
+                                               noop_flag, static_cast<cudaStream_t>(stream)));
+}
+
+int fp8_amax_and_scale_update(float* amax_history, float* scale, float* scale_inv,
+                              int hist_len, int n, int fmt, int margin,
+                              const float* noop_flag, void* stream) {
+    return fp8_amax_and_scale_update_ex(amax_history, scale, scale_inv, hist_len, n, fmt, margin,
+                                        CT_AMAX_MAX, noop_flag, stream);
 }
 
 int fp8_transpose(const void* in, int64_t rows, int64_t cols, void* out, const float* noop_flag,

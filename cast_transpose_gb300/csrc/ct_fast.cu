@@ -274,6 +274,7 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
     int64_t rows = 0, cols = 0;
     uint8_t* out = nullptr;
     uint8_t* out_t = nullptr;
+    int tfmt = 0;               // per-tensor format (list launches with FMT < 0)
     uint32_t amax_pair = 0;     // running bf16 magnitude max (pair form)
     float cs[8];                // dbias: column sums of this thread's 8 columns over
 #pragma unroll                  // the current run down a strip
@@ -310,6 +311,7 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
                 cols = p.t[cur].cols;
                 out = p.t[cur].out;
                 out_t = p.t[cur].out_t;
+                tfmt = p.t[cur].fmt;
             }
             seg = inf.seg;
             seg_end = inf.seg_end != 0;
@@ -349,7 +351,10 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
                         cs[4] += dev::bf16_lo(v[j].z); cs[5] += dev::bf16_hi(v[j].z);
                         cs[6] += dev::bf16_lo(v[j].w); cs[7] += dev::bf16_hi(v[j].w);
                     }
-                    const uint2 q8 = dev::cast8<FMT>(v[j], scale);
+                    // FMT < 0: the format is the tensor's own (uniform per tile)
+                    const uint2 q8 = FMT >= 0  ? dev::cast8<FMT < 0 ? 0 : FMT>(v[j], scale)
+                                     : tfmt == 0 ? dev::cast8<0>(v[j], scale)
+                                                 : dev::cast8<1>(v[j], scale);
                     if (col_ok && row0 + r < rows)
                         __stcs(reinterpret_cast<uint2*>(qrow + r * cols), q8);
                     if constexpr (WRITE_T)   // words 2c, 2c+1 of row r
@@ -535,6 +540,7 @@ cudaError_t launch_fast(const FastParams<1>& p, int fmt, bool dbias, int variant
 
 cudaError_t launch_fast_list(const FastParams<kMaxListPerLaunch>& p, int fmt,
                              cudaStream_t stream) {
+    if (fmt < 0) return launch_variant<kMaxListPerLaunch, -1, true, false>(p, 8, stream);
     return fmt == 0 ? launch_variant<kMaxListPerLaunch, 0, true, false>(p, 6, stream)
                     : launch_variant<kMaxListPerLaunch, 1, true, false>(p, 7, stream);
 }

@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(128) scale_update_warp_kernel(float* __restric
                                                                 int L, int n, int64_t stride,
                                                                 float fp8_max,
                                                                 float two_pow_margin,
+                                                                int most_recent,
                                                                 const float* noop) {
     dev::pdl_launch_dependents();
     dev::pdl_wait();
@@ -165,7 +166,7 @@ __global__ void __launch_bounds__(128) scale_update_warp_kernel(float* __restric
     const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (i >= n) return;
     dev::update_column_warp(hist + i, stride, L, scale + i, scale_inv + i, fp8_max, two_pow_margin,
-                            threadIdx.x & 31);
+                            threadIdx.x & 31, most_recent);
 }
 
 __global__ void __launch_bounds__(128) scale_update_long_kernel(float* __restrict__ hist,
@@ -174,6 +175,7 @@ __global__ void __launch_bounds__(128) scale_update_long_kernel(float* __restric
                                                                 int L, int n, int64_t stride,
                                                                 float fp8_max,
                                                                 float two_pow_margin,
+                                                                int most_recent,
                                                                 const float* noop) {
     dev::pdl_launch_dependents();
     dev::pdl_wait();
@@ -181,7 +183,7 @@ __global__ void __launch_bounds__(128) scale_update_long_kernel(float* __restric
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     dev::update_column_serial(hist + i, stride, L, scale + i, scale_inv + i, fp8_max,
-                              two_pow_margin);
+                              two_pow_margin, most_recent);
 }
 
 // ---------------------------------------------------------------------------
@@ -303,18 +305,18 @@ cudaError_t launch_dbias_finish(const float* partial, int64_t runs, int64_t cols
 }
 
 cudaError_t launch_scale_update(float* hist, float* scale, float* scale_inv, int hist_len,
-                                int count, int64_t stride, int fmt, int margin,
+                                int count, int64_t stride, int fmt, int margin, int most_recent,
                                 const float* noop, cudaStream_t stream) {
     const float fp8_max = fmt == 0 ? 448.0f : 57344.0f;
     const float two_pow_margin = std::ldexp(1.0f, margin);   // exact for 0 <= margin <= 126
     if (hist_len <= 32 * dev::kUpdateRowsPerLane) {
         const dim3 grid(static_cast<unsigned>((int64_t(count) * 32 + 127) / 128)), block(128);
         return launch_pdl(scale_update_warp_kernel, grid, block, 0, stream, hist, scale, scale_inv,
-                          hist_len, count, stride, fp8_max, two_pow_margin, noop);
+                          hist_len, count, stride, fp8_max, two_pow_margin, most_recent, noop);
     }
     const dim3 grid(static_cast<unsigned>((count + 127) / 128)), block(128);
     return launch_pdl(scale_update_long_kernel, grid, block, 0, stream, hist, scale, scale_inv,
-                      hist_len, count, stride, fp8_max, two_pow_margin, noop);
+                      hist_len, count, stride, fp8_max, two_pow_margin, most_recent, noop);
 }
 
 cudaError_t launch_transpose(const uint8_t* in, int64_t rows, int64_t cols, uint8_t* out,

@@ -33,6 +33,7 @@ struct FastTensor {
     int64_t tile_end;      // one past its last global tile index
     int64_t tile_cols;     // tiles per row of tiles
     int64_t tile_rows;     // rows of tiles
+    int32_t fmt;           // FP8 format (read only by list launches with fmt < 0)
 };
 
 template <int NT>
@@ -86,6 +87,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // requires n == 1 and variant 0.
 cudaError_t launch_fast(const FastParams<1>& p, int fmt, bool dbias, int variant,
                         cudaStream_t stream);
+// fmt < 0: each tensor's own t[i].fmt.
 cudaError_t launch_fast_list(const FastParams<kMaxListPerLaunch>& p, int fmt,
                              cudaStream_t stream);
 
@@ -126,7 +128,7 @@ cudaError_t launch_dbias_finish(const float* partial, int64_t runs, int64_t cols
 // Scale update of `count` columns of a [hist_len, stride] history (scale and
 // scale_inv indexed like the columns).
 cudaError_t launch_scale_update(float* hist, float* scale, float* scale_inv, int hist_len,
-                                int count, int64_t stride, int fmt, int margin,
+                                int count, int64_t stride, int fmt, int margin, int most_recent,
                                 const float* noop, cudaStream_t stream);
 
 // FP8 byte transpose.  `fast` requires rows % 16 == 0, cols % 16 == 0 and

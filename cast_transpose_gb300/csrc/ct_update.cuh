@@ -11,6 +11,7 @@
 //       s finite -- otherwise the old scale stays,
 //   scale_inv = 1 / scale,
 //   then the window slides: row r takes row r-1 (r = L-1 .. 1), row 0 := 0.
+// The "most recent" rule takes a = row 0 alone instead of the maximum.
 // Loads go through L2 (ld.global.cg): the amaxes were merged there by the
 // cast kernels' atomics.
 #pragma once
@@ -50,9 +51,12 @@ __device__ __forceinline__ bool better(float va, int ra, float vb, int rb) {
 // costs one round trip to memory.  All 32 lanes must call it.
 constexpr int kUpdateRowsPerLane = 32;
 
+// most_recent != 0: a is row 0 alone (the "most recent" rule); the window
+// still slides.
 __device__ __forceinline__ void update_column_warp(float* hist, int64_t stride, int L, float* scale,
                                                    float* scale_inv, float fp8_max,
-                                                   float two_pow_margin, int lane) {
+                                                   float two_pow_margin, int lane,
+                                                   int most_recent = 0) {
     float v[kUpdateRowsPerLane];
     float best = __int_as_float(0x7FFFFFFF);
     int best_r = -1;
@@ -68,13 +72,17 @@ __device__ __forceinline__ void update_column_warp(float* hist, int64_t stride, 
             }
         }
     }
+    if (most_recent) {
+        best = v[0];   // lane 0 holds row 0; only lane 0 uses `best` below
+    } else {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xFFFFFFFFu, best, off);
-        const int orr = __shfl_xor_sync(0xFFFFFFFFu, best_r, off);
-        if (orr >= 0 && (best_r < 0 || better(ov, orr, best, best_r))) {
-            best = ov;
-            best_r = orr;
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xFFFFFFFFu, best, off);
+            const int orr = __shfl_xor_sync(0xFFFFFFFFu, best_r, off);
+            if (orr >= 0 && (best_r < 0 || better(ov, orr, best, best_r))) {
+                best = ov;
+                best_r = orr;
+            }
         }
     }
     if (lane == 0) finish_scale(best, s_old, fp8_max, two_pow_margin, scale, scale_inv);
@@ -89,9 +97,10 @@ __device__ __forceinline__ void update_column_warp(float* hist, int64_t stride, 
 // Any L, one thread, sequential scan.
 __device__ __forceinline__ void update_column_serial(float* hist, int64_t stride, int L,
                                                      float* scale, float* scale_inv,
-                                                     float fp8_max, float two_pow_margin) {
+                                                     float fp8_max, float two_pow_margin,
+                                                     int most_recent = 0) {
     float a = __ldcg(hist);
-    for (int r = 1; r < L; ++r) {
+    for (int r = 1; r < L && !most_recent; ++r) {
         if (isnan(a)) break;
         const float v = __ldcg(hist + int64_t(r) * stride);
         if (isnan(v) || v > a) a = v;

@@ -76,6 +76,12 @@ typedef enum {
     CT_E5M2 = 1
 } ct_fp8_format;
 
+/* Rule for the amax that sets the next scale (fp8_amax_and_scale_update_ex). */
+typedef enum {
+    CT_AMAX_MAX = 0,          /* maximum over the whole history window          */
+    CT_AMAX_MOST_RECENT = 1   /* the amax of the step that just ran (row 0) only */
+} ct_amax_algo;
+
 typedef enum {
     CT_OK = 0,
     CT_ERR_NULL = 1,        /* a required pointer is NULL                      */
@@ -175,6 +181,19 @@ int fp8_multi_cast_transpose(const ct_tensor_desc* descs, int n, int fmt,
                              const float* noop_flag, void* stream);
 
 /*
+ * fp8_multi_cast_transpose_ex -- fp8_multi_cast_transpose with one FP8
+ * format per tensor (e.g. E4M3 weights and E5M2 gradients in one launch).
+ *
+ *   fmts       HOST array of n formats (CT_E4M3 / CT_E5M2), read during the
+ *              call only; NULL is CT_ERR_NULL when n > 0
+ *
+ * Everything else as fp8_multi_cast_transpose.  The format is uniform over a
+ * 128x128 tile, so the kernel branches once per tile.
+ */
+int fp8_multi_cast_transpose_ex(const ct_tensor_desc* descs, const int* fmts, int n,
+                                const float* noop_flag, void* stream);
+
+/*
  * fp8_amax_and_scale_update -- the delayed-scaling scale update kernel [B]
  * for n tensors, including the infinite-scale guard.
  *
@@ -199,6 +218,18 @@ int fp8_multi_cast_transpose(const ct_tensor_desc* descs, int n, int fmt,
 int fp8_amax_and_scale_update(float* amax_history, float* scale, float* scale_inv,
                               int hist_len, int n, int fmt, int margin,
                               const float* noop_flag, void* stream);
+
+/*
+ * fp8_amax_and_scale_update_ex -- fp8_amax_and_scale_update with a choice of
+ * the amax rule: CT_AMAX_MAX (the window maximum, as fp8_amax_and_scale_update)
+ * or CT_AMAX_MOST_RECENT (row 0 alone: the scale follows the latest amax, the
+ * older rows only ride along in the window).  Guard, scale_inv and the window
+ * slide are the same.  Errors: as fp8_amax_and_scale_update; an unknown
+ * amax_algo is CT_ERR_ARG.
+ */
+int fp8_amax_and_scale_update_ex(float* amax_history, float* scale, float* scale_inv,
+                                 int hist_len, int n, int fmt, int margin, int amax_algo,
+                                 const float* noop_flag, void* stream);
 
 /*
  * fp8_transpose -- byte transpose of an existing FP8 tensor: the lazy

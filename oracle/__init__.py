@@ -69,6 +69,9 @@ def lib() -> ctypes.CDLL:
             L.oracle_fp8_transpose.argtypes = [c.c_void_p, c.c_int64, c.c_int64, c.c_void_p]
             L.oracle_amax_and_scale_update.argtypes = [c.c_void_p, c.c_void_p, c.c_void_p,
                                                        c.c_int, c.c_int, c.c_int, c.c_int]
+            L.oracle_amax_and_scale_update_algo.argtypes = [c.c_void_p, c.c_void_p, c.c_void_p,
+                                                            c.c_int, c.c_int, c.c_int, c.c_int,
+                                                            c.c_int]
             _lib = L
     return _lib
 
@@ -146,13 +149,23 @@ def fp8_transpose(q: np.ndarray) -> np.ndarray:
     return out
 
 
-def amax_and_scale_update(hist, scale, scale_inv, fmt: int, margin: int = 0):
-    """Return updated copies (hist [L, n], scale [n], scale_inv [n])."""
+AMAX_MAX = 0
+AMAX_MOST_RECENT = 1
+
+
+def amax_and_scale_update(hist, scale, scale_inv, fmt: int, margin: int = 0,
+                          algo: int = AMAX_MAX):
+    """Return updated copies (hist [L, n], scale [n], scale_inv [n]).
+    algo: AMAX_MAX (window maximum) or AMAX_MOST_RECENT (row 0 only)."""
     hist = np.array(hist, dtype=np.float32, copy=True, order="C")
     scale = np.array(scale, dtype=np.float32, copy=True)
     scale_inv = np.array(scale_inv, dtype=np.float32, copy=True)
     L, n = hist.shape
     assert scale.shape == (n,) and scale_inv.shape == (n,)
-    lib().oracle_amax_and_scale_update(_ptr(hist), _ptr(scale), _ptr(scale_inv),
-                                       L, n, fmt, margin)
+    if algo == AMAX_MAX:
+        lib().oracle_amax_and_scale_update(_ptr(hist), _ptr(scale), _ptr(scale_inv),
+                                           L, n, fmt, margin)
+    else:
+        lib().oracle_amax_and_scale_update_algo(_ptr(hist), _ptr(scale), _ptr(scale_inv),
+                                                L, n, fmt, margin, 1)
     return hist, scale, scale_inv

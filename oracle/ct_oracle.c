@@ -233,15 +233,16 @@ void oracle_fp8_transpose(const uint8_t* in, int64_t rows, int64_t cols, uint8_t
  *            finite, in which case the old scale is kept
  *   scale_inv = 1 / scale
  *   then the window slides: row r takes row r-1 (r = L-1 .. 1), row 0 := 0.
+ * With most_recent != 0, a is row 0 alone (the "most recent" amax rule).
  */
-void oracle_amax_and_scale_update(float* hist, float* scale, float* scale_inv,
-                                  int L, int n, int fmt, int margin)
+void oracle_amax_and_scale_update_algo(float* hist, float* scale, float* scale_inv,
+                                       int L, int n, int fmt, int margin, int most_recent)
 {
     const float fp8_max = format_of(fmt).maxval;
     const float two_pow_margin = ldexpf(1.0f, margin);
     for (int i = 0; i < n; ++i) {
         float a = hist[i];
-        for (int r = 1; r < L; ++r) {
+        for (int r = 1; r < L && !most_recent; ++r) {
             float v = hist[(int64_t)r * n + i];
             if (isnan(a)) break;
             if (isnan(v) || v > a) a = v;
@@ -257,4 +258,11 @@ void oracle_amax_and_scale_update(float* hist, float* scale, float* scale_inv,
             hist[(int64_t)r * n + i] = hist[(int64_t)(r - 1) * n + i];
         hist[i] = 0.0f;
     }
+}
+
+/* The update with the window maximum (most_recent = 0). */
+void oracle_amax_and_scale_update(float* hist, float* scale, float* scale_inv,
+                                  int L, int n, int fmt, int margin)
+{
+    oracle_amax_and_scale_update_algo(hist, scale, scale_inv, L, n, fmt, margin, 0);
 }

@@ -153,3 +153,16 @@ def test_python_binding_rejects_cpu_tensors():
 def test_selftest_rejects_bad_limits(L):
     assert L.ct_selftest_bounded_wait(0, None) == CT_ERR_ARG
     assert L.ct_selftest_bounded_wait(2000000, None) == CT_ERR_ARG
+
+
+def test_update_ex_rejects_unknown_algo(L):
+    assert L.fp8_amax_and_scale_update_ex(X, S, SI, 16, 4, 0, 0, 2, None, None) == CT_ERR_ARG
+    assert L.fp8_amax_and_scale_update_ex(X, S, SI, 16, 0, 0, 0, 1, None, None) == CT_OK
+
+
+def test_multi_ex_rejects(L):
+    arr = (ct._Desc * 1)(_desc())
+    assert L.fp8_multi_cast_transpose_ex(arr, None, 1, None, None) == CT_ERR_NULL
+    bad = (ctypes.c_int * 1)(7)
+    assert L.fp8_multi_cast_transpose_ex(arr, bad, 1, None, None) == CT_ERR_FORMAT
+    assert L.fp8_multi_cast_transpose_ex(None, None, 0, None, None) == CT_OK

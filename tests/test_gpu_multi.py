@@ -122,3 +122,32 @@ def test_multi_48_tensor_list_with_update():
     assert np.array_equal(scales.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
     assert np.array_equal(recipe_sinv.cpu().numpy().view(np.uint32), si_ref.view(np.uint32))
     assert np.all(s_ref[list(workloads.MULTI_ZERO)] == 1.0)     # amax 0: scale kept
+
+
+def test_per_tensor_formats_in_one_launch():
+    """fp8_multi_cast_transpose_ex: E4M3 and E5M2 entries mixed in one list
+    (TMA-path and general-path shapes)."""
+    shapes = [(256, 384), (512, 128), (33, 65), (1024, 1040), (128, 4096), (96, 96)]
+    fmts = [ct.E4M3, ct.E5M2, ct.E5M2, ct.E4M3, ct.E5M2, ct.E4M3]
+    xs_cpu = [workloads.normal_bf16(r, c, 300.0, 700 + i) for i, (r, c) in enumerate(shapes)]
+    n = len(xs_cpu)
+    scales = torch.tensor([1.0, 4.0, 0.5, 2.0, 8.0, 1.0], device="cuda")
+    amax = torch.zeros(n, device="cuda")
+    sinv = torch.zeros(n, device="cuda")
+    outs = [Guarded(x.numel()) for x in xs_cpu]
+    outs_t = [Guarded(x.numel()) for x in xs_cpu]
+    ct.fp8_multi_cast_transpose_ex([x.cuda() for x in xs_cpu], [scales[i:i + 1] for i in range(n)],
+                                   [amax[i:i + 1] for i in range(n)],
+                                   [sinv[i:i + 1] for i in range(n)], [o.t for o in outs],
+                                   [o.t for o in outs_t], fmts)
+    torch.cuda.synchronize()
+    a, si = amax.cpu().numpy(), sinv.cpu().numpy()
+    for i, x in enumerate(xs_cpu):
+        r, c = x.shape
+        outs[i].check()
+        outs_t[i].check()
+        ref = oracle.cast_transpose(x, float(scales[i].item()), fmts[i])
+        assert np.array_equal(outs[i].numpy().reshape(r, c), ref["q"]), i
+        assert np.array_equal(outs_t[i].numpy().reshape(c, r), ref["qt"]), i
+        assert f32_bits(a[i]) == f32_bits(ref["amax"]), i
+        assert f32_bits(si[i]) == f32_bits(ref["scale_inv"]), i

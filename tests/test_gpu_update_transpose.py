@@ -35,18 +35,19 @@ def _history(L, n, seed):
     return h
 
 
+@pytest.mark.parametrize("algo", [ct.AMAX_MAX, ct.AMAX_MOST_RECENT])
 @pytest.mark.parametrize("fmt", [ct.E4M3, ct.E5M2])
 @pytest.mark.parametrize("L,n,margin", [(16, 1, 0), (16, 48, 0), (1, 7, 0), (1024, 300, 3),
-                                        (4, 1000, 126), (2, 8, 1)])
-def test_update_matches_oracle(fmt, L, n, margin):
+                                        (4, 1000, 126), (2, 8, 1), (1100, 5, 0)])
+def test_update_matches_oracle(fmt, L, n, margin, algo):
     h = _history(L, max(n, 6), seed=L * 1000 + n)[:, :n].copy()
     rng = np.random.default_rng(n)
     s = (rng.random(n) * 100 + 0.01).astype(np.float32)
     si = np.zeros(n, np.float32)
     hd, sd, sid = torch.from_numpy(h).cuda(), torch.from_numpy(s).cuda(), torch.from_numpy(si).cuda()
     for step in range(3):
-        ct.fp8_amax_and_scale_update(hd, sd, sid, fmt, margin)
-        h, s, si = oracle.amax_and_scale_update(h, s, si, fmt, margin)
+        ct.fp8_amax_and_scale_update_ex(hd, sd, sid, fmt, margin, amax_algo=algo)
+        h, s, si = oracle.amax_and_scale_update(h, s, si, fmt, margin, algo=algo)
         torch.cuda.synchronize()
         assert np.array_equal(hd.cpu().numpy().view(np.uint32), h.view(np.uint32)), step
         assert np.array_equal(sd.cpu().numpy().view(np.uint32), s.view(np.uint32)), step

@@ -106,3 +106,28 @@ def test_nan_in_history_propagates(oracle_lib):
     h, scale, _ = oracle.amax_and_scale_update(hist, s, s, oracle.E4M3, 0)
     assert list(scale) == [1.0, 1.0]
     assert np.array_equal(h[1:], hist[:-1], equal_nan=True)
+
+
+def test_most_recent_ignores_older_rows(oracle_lib):
+    # rows 1..: a spike of 100 that the window maximum would use
+    hist = np.array([[2.0, 0.0, np.nan], [100.0, 100.0, 1.0], [7.0, 3.0, 1.0]], dtype=np.float32)
+    s = np.array([1.0, 5.0, 6.0], np.float32)
+    h, scale, sinv = oracle.amax_and_scale_update(hist, s, s, oracle.E4M3, 0,
+                                                  algo=oracle.AMAX_MOST_RECENT)
+    assert scale[0] == np.float32(224.0)            # 448 / 2, the spike ignored
+    assert scale[1] == 5.0                           # row 0 is 0: the scale stays
+    assert scale[2] == 6.0                           # row 0 is NaN: the scale stays
+    assert _is_correctly_rounded(sinv[0], 1 / Fraction(224))
+    assert np.array_equal(h[1:], hist[:-1], equal_nan=True) and np.all(h[0] == 0)
+    _, smax, _ = oracle.amax_and_scale_update(hist, s, s, oracle.E4M3, 0)
+    assert smax[0] == np.float32(4.48)               # the window maximum uses the spike
+
+
+def test_most_recent_equals_max_for_history_of_one(oracle_lib):
+    rng = np.random.default_rng(1)
+    hist = np.abs(rng.standard_normal((1, 50))).astype(np.float32)
+    s = np.ones(50, np.float32)
+    a = oracle.amax_and_scale_update(hist, s, s, oracle.E5M2, 3)
+    b = oracle.amax_and_scale_update(hist, s, s, oracle.E5M2, 3, algo=oracle.AMAX_MOST_RECENT)
+    for u, v in zip(a, b):
+        assert np.array_equal(u.view(np.uint32), v.view(np.uint32))
