@@ -52,7 +52,10 @@
  *     row lengths are multiples of 16 bytes and 16-byte-aligned buffers take
  *     the TMA-staged fast path, everything else a slower general kernel
  *     with identical results.
- *   - Calls are thread-safe; the library keeps no per-call state.
+ *   - Calls are thread-safe; the library keeps no per-call state.  The first
+ *     call of an entry point on a device also sets its kernels' shared-memory
+ *     limit (cudaFuncSetAttribute, once per device): make that first call
+ *     outside stream capture, as one makes a warm-up call before capturing.
  *   - Kernels are launched as programmatic dependents of the previous kernel
  *     in the stream: a cast kernel may start fetching its bf16 input while
  *     the library's preceding kernel on that stream is still finishing.

@@ -144,3 +144,39 @@ def test_graph_multi_update_transpose_with_noop():
     for b0, b1 in zip(snap, after):
         assert np.array_equal(b0, b1)
     assert ct.device_error() == 0
+
+
+def test_concurrent_calls_from_two_threads_on_two_streams():
+    """The library keeps no per-call state: two host threads casting different
+    tensors on their own streams at the same time both get exact results."""
+    import threading
+    xs_cpu = [workloads.normal_bf16(4096, 2048, 1.0 + i, 900 + i) for i in range(2)]
+    xs = [x.cuda() for x in xs_cpu]
+    res = [None, None]
+    errs = []
+
+    def work(i):
+        try:
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                q, qt = ct.empty_outputs(xs[i])
+                a, si = scalar(0.0), scalar(0.0)
+                for _ in range(20):
+                    a.zero_()
+                    ct.fp8_cast_transpose(xs[i], scalar(0.5 * (i + 1)), a, si, q, qt,
+                                          ct.E4M3 if i == 0 else ct.E5M2)
+                st.synchronize()
+                res[i] = (q.cpu().numpy(), qt.cpu().numpy(), a.item())
+        except Exception as e:      # surfaced below
+            errs.append(e)
+
+    ts = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errs, errs
+    for i in range(2):
+        ref = oracle.cast_transpose(xs_cpu[i], 0.5 * (i + 1), ct.E4M3 if i == 0 else ct.E5M2)
+        assert np.array_equal(res[i][0], ref["q"]) and np.array_equal(res[i][1], ref["qt"])
+        assert f32_bits(res[i][2]) == f32_bits(ref["amax"])
