@@ -170,3 +170,51 @@ def test_more_than_2_to_31_elements():
         assert torch.equal(qt[c0:c0 + 5632], q[:, c0:c0 + 5632].t())
     assert f32_bits(a.item()) == f32_bits(oracle.amax(x.cpu()))
     assert si.item() == 0.5
+
+
+def test_weight_step_as_benchmarked():
+    """The benchmark's launch configuration: the 4096x4096 step (x * 2^k for
+    k = -4..3, each cast followed by the update) captured once in a CUDA
+    graph and replayed, with programmatic dependent launch between the 16
+    kernels; one eager warm-up step, then two replays.  Every output of the
+    last replay and the history/scale state match the oracle."""
+    L = 16
+    base = workloads.weight_matrix("cuda")
+    xs = [workloads.weight_rescaled(base, k) for k in workloads.WEIGHT_EXPONENTS]
+    outs = [ct.empty_outputs(x) for x in xs]
+    hist = torch.zeros(L, 1, device="cuda")
+    scale, rsi = scalar(1.0), scalar(1.0)
+    tsi = torch.zeros(len(xs), device="cuda")
+
+    def step():
+        for k, x in enumerate(xs):
+            ct.fp8_cast_transpose(x, scale, hist[0], tsi[k:k + 1], outs[k][0], outs[k][1], ct.E4M3)
+            ct.fp8_amax_and_scale_update(hist, scale, rsi, ct.E4M3, 0)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    xs_cpu = [x.cpu() for x in xs]
+    h = np.zeros((L, 1), np.float32)
+    s = np.ones(1, np.float32)
+    si = np.ones(1, np.float32)
+    for rep in range(3):
+        for k in range(len(xs)):
+            r = oracle.cast_transpose(xs_cpu[k], float(s[0]), ct.E4M3, want_qt=(rep == 2))
+            if rep == 2:
+                assert np.array_equal(outs[k][0].cpu().numpy(), r["q"]), k
+                assert np.array_equal(outs[k][1].cpu().numpy(), r["qt"]), k
+                assert f32_bits(tsi[k].item()) == f32_bits(r["scale_inv"]), k
+            h[0, 0] = r["amax"]
+            h, s, si = oracle.amax_and_scale_update(h, s, si, ct.E4M3, 0)
+    assert np.array_equal(hist.cpu().numpy().view(np.uint32), h.view(np.uint32))
+    assert f32_bits(scale.item()) == f32_bits(s[0]) and f32_bits(rsi.item()) == f32_bits(si[0])
