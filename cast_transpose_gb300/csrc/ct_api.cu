@@ -9,12 +9,15 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cstdint>
 #include <cstring>
 #include <mutex>
 #include <vector>
 
 namespace {
 
+using ct::DirectParams;
 using ct::FastParams;
 using ct::FastTensor;
 
@@ -132,6 +135,19 @@ int cast_impl(const void* x, int64_t rows, int64_t cols, const float* scale, flo
               const float* noop, cudaStream_t stream, int64_t* runs_out = nullptr) {
     const int64_t R = (rows + ct::kTileRows - 1) / ct::kTileRows;
     if (fast_eligible(x, rows, cols, out, out_t)) {
+        const int64_t tiles = R * ((cols + ct::kTileCols - 1) / ct::kTileCols);
+        if (tiles >= ct::kDirectMinTiles && tiles <= INT32_MAX) {
+            DirectParams<1> d;
+            std::memset(&d, 0, sizeof(d));
+            d.x[0] = static_cast<const uint16_t*>(x);
+            fill_tensor(d.t[0], out, out_t, scale, amax, scale_inv, rows, cols, 0);
+            d.n = 1;
+            d.total_tiles = tiles;
+            d.noop = noop;
+            d.partial = partial;
+            if (runs_out) *runs_out = R;
+            return cuda_status(ct::launch_direct(d, fmt, partial != nullptr, out_t ? 0 : 1, stream));
+        }
         FastParams<1> p;
         std::memset(&p, 0, sizeof(p));
         if (!encode_bf16_map(&p.map[0], x, rows, cols)) return CT_ERR_CUDA;
@@ -275,11 +291,38 @@ int multi_impl(const ct_tensor_desc* descs, const int* fmts, int n, int fmt,
         (fast_eligible(d.x, d.rows, d.cols, d.out, d.out_t) ? fast : general).push_back(i);
     }
     for (size_t base = 0; base < fast.size(); base += ct::kMaxListPerLaunch) {
+        const size_t end = std::min(fast.size(), base + size_t(ct::kMaxListPerLaunch));
+        int64_t chunk_tiles = 0;
+        for (size_t k = base; k < end; ++k) {
+            const ct_tensor_desc& d = descs[fast[k]];
+            chunk_tiles += row_tiles(d.rows) * ((d.cols + ct::kTileCols - 1) / ct::kTileCols);
+        }
+        if (chunk_tiles >= ct::kDirectMinTiles && chunk_tiles <= INT32_MAX) {
+            static thread_local DirectParams<ct::kMaxListPerLaunch> q;
+            std::memset(&q, 0, sizeof(q));
+            int64_t tiles = 0;
+            int m = 0;
+            for (size_t k = base; k < end; ++k, ++m) {
+                const ct_tensor_desc& d = descs[fast[k]];
+                q.x[m] = static_cast<const uint16_t*>(d.x);
+                fill_tensor(q.t[m], d.out, d.out_t, d.scale, d.amax, d.scale_inv, d.rows, d.cols,
+                            tiles);
+                q.t[m].fmt = fmt_of(fast[k]);
+                tiles = q.t[m].tile_end;
+            }
+            q.n = m;
+            q.total_tiles = tiles;
+            q.noop = noop_flag;
+            q.partial = nullptr;
+            const int st = cuda_status(ct::launch_direct_list(q, fmts ? -1 : fmt, s));
+            if (st != CT_OK) return st;
+            continue;
+        }
         static thread_local FastParams<ct::kMaxListPerLaunch> p;
         std::memset(&p, 0, sizeof(p));
         int64_t tiles = 0;
         int m = 0;
-        for (size_t k = base; k < fast.size() && m < ct::kMaxListPerLaunch; ++k, ++m) {
+        for (size_t k = base; k < end; ++k, ++m) {
             const ct_tensor_desc& d = descs[fast[k]];
             if (!encode_bf16_map(&p.map[m], d.x, d.rows, d.cols)) return CT_ERR_CUDA;
             fill_tensor(p.t[m], d.out, d.out_t, d.scale, d.amax, d.scale_inv, d.rows, d.cols, tiles);

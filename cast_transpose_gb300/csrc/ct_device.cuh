@@ -181,6 +181,13 @@ __device__ __forceinline__ void transpose4x4(uint32_t r0, uint32_t r1, uint32_t 
     c3 = __byte_perm(t2, t3, 0x7632);
 }
 
+// Shared-memory layout of the FP8 copy of a 128x128 tile used for the
+// transposed write: 128 rows of 32 words (4 FP8 codes each); word wd of row r
+// lives at wd ^ swz(r).  The XOR spreads the 8 row blocks that the transpose
+// pass reads at once over all 32 banks, and keeps the two words of every
+// 8-byte row store adjacent (swz is even).
+__device__ __forceinline__ int swz(int r) { return 2 * ((r >> 3) & 15); }
+
 // Max of the two bf16 magnitudes (sign cleared) of a packed pair, kept as a
 // pair: one AND and one native 16x2 unsigned max per word.
 __device__ __forceinline__ uint32_t absmax_pair(uint32_t acc, uint32_t w) {

@@ -1,0 +1,206 @@
+// ct_direct.cu -- one-tile-per-CTA cast-transpose with direct vector loads (sm_103a).
+//
+// Operation ("[PyTorch] cuda graph support", DbiasCastTranspose example;
+// "[PyTorch] Refactor FP8 workspaces in linear modules", Motivations): the
+// same as the TMA kernel of ct_fast.cu -- q = fp8(x * scale), its transpose
+// qT, max|x| max-merged into *amax, scale_inv = 1 / scale and (dbias) the
+// fp32 column sums of x -- for launches large enough to fill the GPU many
+// times over.
+//
+// Design: the CTA of 256 threads that owns tile (rt, ct) issues all of its
+// 128x128 bf16 tile as eight 16-byte loads per thread at once (16 threads
+// cover one 256-byte row segment, 128 KB in flight per SM at 4 resident
+// CTAs), then
+//   * pass 1: converts each 8-element vector to 8 FP8 codes, stores them to q
+//     (16 threads write one 128-byte line) and into the XOR-swizzled FP8 copy
+//     of the tile in shared memory (dev::swz); keeps the amax as a SIMD max
+//     of bf16 magnitudes and, for dbias, 8 column sums per thread;
+//   * one __syncthreads;
+//   * pass 2: each thread gathers a 16-row x 4-column byte block of the copy,
+//     transposes it with byte permutes and writes four 16-byte vectors of qT
+//     (8 threads write one 128-byte line).
+// No pipeline state crosses tiles, so the kernel has no waits; the latency of
+// one tile's loads is hidden by the other resident CTAs.  Grids are the tile
+// count (thousands of CTAs, many waves of 152 SMs x 4); the TMA kernel keeps
+// the launches too small for that to pay.
+#include "ct_device.cuh"
+#include "ct_internal.h"
+
+#include <climits>
+
+namespace ct {
+namespace {
+
+constexpr int kDirectThreads = 256;
+#ifndef CT_DIRECT_MINB
+#define CT_DIRECT_MINB 4
+#endif
+constexpr int kDirectMinBlocks = CT_DIRECT_MINB;
+constexpr int kDirectWarps = kDirectThreads / 32;
+
+// The tensor of a list launch that owns global tile `tile`: the last entry
+// whose first tile is <= tile (entries are non-empty and in tile order).
+template <int NT>
+__device__ __forceinline__ int owner(const DirectParams<NT>& p, int64_t tile) {
+    if constexpr (NT == 1) {
+        return 0;
+    } else {
+        int lo = 0, hi = p.n - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.t[mid].tile_begin <= tile) lo = mid;
+            else hi = mid - 1;
+        }
+        return lo;
+    }
+}
+
+template <int NT, int FMT, bool WRITE_T, bool DBIAS>
+__global__ void __launch_bounds__(kDirectThreads, kDirectMinBlocks)
+    direct_cast_transpose_kernel(const __grid_constant__ DirectParams<NT> p) {
+    // The next kernel of the stream may be scheduled as soon as this grid's
+    // last wave is resident; it waits for this grid on the device.
+    dev::pdl_launch_dependents();
+    dev::pdl_wait();
+    if (p.noop != nullptr && *p.noop != 0.0f) return;
+
+    __shared__ __align__(16) uint8_t sq[WRITE_T ? kTileRows * kTileCols : 16];
+    __shared__ __align__(16) float colsum[DBIAS ? kDirectWarps * kTileCols : 4];
+    __shared__ unsigned s_amax[kDirectWarps];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t tile = blockIdx.x;
+    const int ti = owner(p, tile);
+    const FastTensor& T = p.t[ti];
+    const int64_t rows = T.rows, cols = T.cols;
+    const int64_t local = tile - T.tile_begin;
+    const int64_t rt = local / T.tile_cols;
+    const int64_t row0 = rt * kTileRows, col0 = (local - rt * T.tile_cols) * kTileCols;
+    const float scale = *T.scale;
+    const int tfmt = T.fmt;
+
+    // pass-1 mapping: column chunk c (8 columns), rows rg + 16 * it
+    const int c = tid & 15, rg = tid >> 4;
+    const bool col_ok = col0 + 8 * c < cols;   // cols % 8 == 0: the chunk is whole
+    const uint16_t* xin = p.x[ti] + col0 + 8 * c;
+    uint4 v[8];
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int64_t row = row0 + rg + 16 * it;
+        v[it] = (col_ok && row < rows) ? __ldcs(reinterpret_cast<const uint4*>(xin + row * cols))
+                                       : make_uint4(0u, 0u, 0u, 0u);
+    }
+
+    uint32_t amax_pair = 0;
+    float cs[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) cs[j] = 0.0f;
+    uint8_t* qrow = T.out + row0 * cols + col0 + 8 * c;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int r = rg + 16 * it;
+        amax_pair = dev::absmax_pair(amax_pair, v[it].x);
+        amax_pair = dev::absmax_pair(amax_pair, v[it].y);
+        amax_pair = dev::absmax_pair(amax_pair, v[it].z);
+        amax_pair = dev::absmax_pair(amax_pair, v[it].w);
+        if constexpr (DBIAS) {
+            cs[0] += dev::bf16_lo(v[it].x); cs[1] += dev::bf16_hi(v[it].x);
+            cs[2] += dev::bf16_lo(v[it].y); cs[3] += dev::bf16_hi(v[it].y);
+            cs[4] += dev::bf16_lo(v[it].z); cs[5] += dev::bf16_hi(v[it].z);
+            cs[6] += dev::bf16_lo(v[it].w); cs[7] += dev::bf16_hi(v[it].w);
+        }
+        // FMT < 0: the tensor's own format (uniform over the CTA)
+        const uint2 q8 = FMT >= 0  ? dev::cast8<FMT < 0 ? 0 : FMT>(v[it], scale)
+                         : tfmt == 0 ? dev::cast8<0>(v[it], scale)
+                                     : dev::cast8<1>(v[it], scale);
+        if (col_ok && row0 + r < rows) __stcs(reinterpret_cast<uint2*>(qrow + r * cols), q8);
+        if constexpr (WRITE_T)   // words 2c, 2c+1 of row r
+            *reinterpret_cast<uint2*>(sq + r * kTileCols + ((2 * c) ^ dev::swz(r)) * 4) = q8;
+    }
+    const unsigned m = __reduce_max_sync(0xFFFFFFFFu, dev::pair_to_f32_bits(amax_pair));
+    if (lane == 0) s_amax[warp] = m;
+    if constexpr (DBIAS) {   // fold the warp's two row groups (lanes l, l + 16)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) cs[j] += __shfl_xor_sync(0xFFFFFFFFu, cs[j], 16);
+        if (lane < 16) {
+            float4* dst = reinterpret_cast<float4*>(colsum + warp * kTileCols + 8 * c);
+            dst[0] = make_float4(cs[0], cs[1], cs[2], cs[3]);
+            dst[1] = make_float4(cs[4], cs[5], cs[6], cs[7]);
+        }
+    }
+    __syncthreads();
+
+    if (tid == 0) {
+        unsigned a = s_amax[0];
+#pragma unroll
+        for (int w = 1; w < kDirectWarps; ++w) a = a > s_amax[w] ? a : s_amax[w];
+        if (a != 0) atomicMax(reinterpret_cast<unsigned*>(T.amax), a);
+        if (local == 0) *T.scale_inv = __fdiv_rn(1.0f, scale);
+    }
+    if constexpr (DBIAS) {   // one partial row per tile row, warps summed in order
+        if (tid < kTileCols && col0 + tid < cols) {
+            float sum = colsum[tid];
+#pragma unroll
+            for (int w = 1; w < kDirectWarps; ++w) sum += colsum[w * kTileCols + tid];
+            p.partial[rt * cols + col0 + tid] = sum;
+        }
+    }
+
+    if constexpr (WRITE_T) {
+        // pass-2 mapping: rows 16 * b .. 16 * b + 15, 4-column word w
+        const int b = lane & 7, w = warp * 4 + (lane >> 3);
+        const uint32_t* sq32 = reinterpret_cast<const uint32_t*>(sq);
+        uint32_t rw[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int r = 16 * b + j;
+            rw[j] = sq32[r * (kTileCols / 4) + (w ^ dev::swz(r))];
+        }
+        uint32_t o[4][4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+            dev::transpose4x4(rw[4 * g], rw[4 * g + 1], rw[4 * g + 2], rw[4 * g + 3], o[0][g],
+                              o[1][g], o[2][g], o[3][g]);
+        const int64_t row = row0 + 16 * b;   // rows % 16 == 0: the block is whole
+        if (row < rows) {
+#pragma unroll
+            for (int kq = 0; kq < 4; ++kq) {
+                const int64_t col = col0 + 4 * w + kq;
+                if (col < cols)
+                    __stcs(reinterpret_cast<uint4*>(T.out_t + col * rows + row),
+                           make_uint4(o[kq][0], o[kq][1], o[kq][2], o[kq][3]));
+            }
+        }
+    }
+}
+
+template <int NT, int FMT, bool WRITE_T, bool DBIAS>
+cudaError_t launch_one(const DirectParams<NT>& p, cudaStream_t stream) {
+    if (p.total_tiles <= 0 || p.total_tiles > INT_MAX) return cudaErrorInvalidValue;
+    return launch_pdl(direct_cast_transpose_kernel<NT, FMT, WRITE_T, DBIAS>,
+                      dim3(static_cast<unsigned>(p.total_tiles)), dim3(kDirectThreads), 0, stream,
+                      p);
+}
+
+}  // namespace
+
+cudaError_t launch_direct(const DirectParams<1>& p, int fmt, bool dbias, int variant,
+                          cudaStream_t stream) {
+    if (variant == 1)
+        return fmt == 0 ? launch_one<1, 0, false, false>(p, stream)
+                        : launch_one<1, 1, false, false>(p, stream);
+    if (dbias)
+        return fmt == 0 ? launch_one<1, 0, true, true>(p, stream)
+                        : launch_one<1, 1, true, true>(p, stream);
+    return fmt == 0 ? launch_one<1, 0, true, false>(p, stream)
+                    : launch_one<1, 1, true, false>(p, stream);
+}
+
+cudaError_t launch_direct_list(const DirectParams<kMaxListPerLaunch>& p, int fmt,
+                               cudaStream_t stream) {
+    if (fmt < 0) return launch_one<kMaxListPerLaunch, -1, true, false>(p, stream);
+    return fmt == 0 ? launch_one<kMaxListPerLaunch, 0, true, false>(p, stream)
+                    : launch_one<kMaxListPerLaunch, 1, true, false>(p, stream);
+}
+
+}  // namespace ct

@@ -58,11 +58,8 @@ static_assert(kFastThreads == 256 || kFastThreads == 512, "256 or 512 threads");
 constexpr int kWarps = kFastThreads / 32;
 constexpr int kColsumFloats = kWarps * kTileCols;         // [warp][col]
 
-// Shared-memory layout of the FP8 copy of a tile: 128 rows of 32 words (4
-// FP8 codes each); word wd of row r lives at wd ^ swz(r).  The XOR spreads
-// the 8 row blocks that pass 2 reads at once over all 32 banks, and keeps
-// the two words of every 8-byte pass-1 store adjacent.
-__device__ __forceinline__ int swz(int r) { return 2 * ((r >> 3) & 15); }
+// Shared-memory layout of the FP8 copy of a tile: see dev::swz.
+using dev::swz;
 
 // Where a staged tile came from.  Written by the producer thread before it
 // arms the stage's mbarrier, read by the consumers after the barrier phase

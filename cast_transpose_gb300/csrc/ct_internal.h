@@ -91,6 +91,33 @@ cudaError_t launch_fast(const FastParams<1>& p, int fmt, bool dbias, int variant
 cudaError_t launch_fast_list(const FastParams<kMaxListPerLaunch>& p, int fmt,
                              cudaStream_t stream);
 
+// Direct-load path (ct_direct.cu): one CTA per 128x128 tile, x read with
+// plain 16-byte loads; same eligibility as the TMA path (rows % 16 == 0,
+// cols % 16 == 0, 16-byte aligned x, out and out_t).  Chosen for launches of
+// at least kDirectMinTiles tiles (at most INT32_MAX), where it sustains a
+// higher read+write rate than the persistent TMA kernel; the persistent
+// kernel keeps the smaller launches, whose tiles it spreads evenly and whose
+// first loads it overlaps with the previous kernel.
+template <int NT>
+struct DirectParams {
+    const uint16_t* x[NT];  // bf16 inputs
+    FastTensor t[NT];
+    int n;
+    int64_t total_tiles;
+    const float* noop;      // nullable device flag
+    float* partial;         // dbias partials [ceil(rows/128), cols] (one row per tile row), or null
+};
+#ifndef CT_DIRECT_MIN_TILES
+#define CT_DIRECT_MIN_TILES 2048
+#endif
+constexpr int64_t kDirectMinTiles = CT_DIRECT_MIN_TILES;
+// `variant`: 0 = cast + transpose, 1 = cast only; `dbias` requires variant 0.
+cudaError_t launch_direct(const DirectParams<1>& p, int fmt, bool dbias, int variant,
+                          cudaStream_t stream);
+// fmt < 0: each tensor's own t[i].fmt.
+cudaError_t launch_direct_list(const DirectParams<kMaxListPerLaunch>& p, int fmt,
+                               cudaStream_t stream);
+
 // General path.
 cudaError_t launch_general(const GeneralArgs& a, int fmt, cudaStream_t stream);
 

@@ -1,0 +1,178 @@
+"""GPU parity of the large-launch kernel (one 128x128 tile per CTA, direct
+16-byte loads) that the library picks for launches of 2048 tiles or more:
+ragged shapes (row and column tile counts not multiples of 128), every entry
+point that reaches it (cast + transpose, cast only, dbias, tensor lists with
+one or per-tensor formats), the noop flag and graph replay.  Bit-exact
+against the oracle; db within the dbias tolerance.
+"""
+import numpy as np
+import pytest
+import torch
+
+import cast_transpose_gb300 as ct
+import oracle
+from cast_transpose_gb300 import workloads
+from gpu_util import Guarded, assert_same_cast, cast_transpose_gpu, dbias_tolerance_ok, f32_bits, scalar
+
+pytestmark = pytest.mark.gpu
+
+# >= 2048 tiles of 128x128, neither dimension a multiple of 128
+RAGGED = [(4112, 8208), (2064, 16400), (16400, 2064)]
+
+
+def _tiles(rows, cols):
+    return -(-rows // 128) * -(-cols // 128)
+
+
+@pytest.fixture(autouse=True)
+def _no_device_error():
+    ct.device_error(clear=True)
+    yield
+    assert ct.device_error() == 0
+
+
+@pytest.mark.parametrize("fmt", [ct.E4M3, ct.E5M2])
+@pytest.mark.parametrize("shape", RAGGED)
+def test_ragged_cast_transpose(fmt, shape):
+    rows, cols = shape
+    assert _tiles(rows, cols) >= 2048
+    x_cpu = workloads.normal_bf16(rows, cols, 50.0, 900 + rows + cols)
+    got = cast_transpose_gpu(x_cpu.cuda(), 2.5, fmt, amax_in=0.125)
+    assert_same_cast(got, oracle.cast_transpose(x_cpu, 2.5, fmt, amax_in=0.125))
+
+
+def test_all_bf16_patterns_tiled():
+    """Every bf16 pattern, repeated to a 4096 x 8192 matrix (2048 tiles)."""
+    base = workloads.bf16_all_patterns().reshape(-1)
+    g = torch.Generator().manual_seed(5)
+    x_cpu = base[torch.randperm(65536, generator=g).repeat(512)].reshape(4096, 8192).contiguous()
+    got = cast_transpose_gpu(x_cpu.cuda(), 3.7, ct.E5M2)
+    assert_same_cast(got, oracle.cast_transpose(x_cpu, float(np.float32(3.7)), ct.E5M2))
+
+
+@pytest.mark.parametrize("fmt", [ct.E4M3, ct.E5M2])
+def test_ragged_cast_only(fmt):
+    rows, cols = RAGGED[0]
+    x_cpu = workloads.normal_bf16(rows, cols, 30.0, 41)
+    q = Guarded(rows * cols)
+    s, a, si = scalar(0.75), scalar(0.0), scalar(0.0)
+    ct.fp8_cast(x_cpu.cuda(), s, a, si, q.t, fmt)
+    torch.cuda.synchronize()
+    q.check()
+    ref = oracle.cast_transpose(x_cpu, 0.75, fmt, want_qt=False)
+    assert np.array_equal(q.numpy().reshape(rows, cols), ref["q"])
+    assert f32_bits(a.item()) == f32_bits(ref["amax"])
+    assert f32_bits(si.item()) == f32_bits(ref["scale_inv"])
+
+
+@pytest.mark.parametrize("fmt", [ct.E4M3, ct.E5M2])
+@pytest.mark.parametrize("shape", RAGGED[:2])
+def test_ragged_dbias(fmt, shape):
+    rows, cols = shape
+    x_cpu = workloads.gradient_matrix("cpu", rows, cols, std=1e-3, outlier_fraction=1e-3)
+    n = rows * cols
+    q, qt = Guarded(n), Guarded(n)
+    db = Guarded(cols, dtype=torch.float32)
+    ws = torch.empty(ct.dbias_workspace_size(rows, cols), dtype=torch.uint8, device="cuda")
+    ws.fill_(0x7F)
+    s, a, si = scalar(4.0), scalar(0.0), scalar(0.0)
+    ct.fp8_dbias_cast_transpose(x_cpu.cuda(), s, a, si, q.t, qt.t, db.t, ws, fmt)
+    torch.cuda.synchronize()
+    for g in (q, qt, db):
+        g.check()
+    ref = oracle.cast_transpose(x_cpu, 4.0, fmt)
+    assert np.array_equal(q.numpy().reshape(rows, cols), ref["q"])
+    assert np.array_equal(qt.numpy().reshape(cols, rows), ref["qt"])
+    assert f32_bits(a.item()) == f32_bits(ref["amax"])
+    assert f32_bits(si.item()) == f32_bits(ref["scale_inv"])
+    assert dbias_tolerance_ok(db.numpy(), oracle.dbias(x_cpu), x_cpu)
+
+
+def test_dbias_deterministic():
+    x = workloads.gradient_matrix("cuda", 4112, 8208)
+    cols = x.shape[1]
+    ws = torch.empty(ct.dbias_workspace_size(*x.shape), dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(2):
+        q, qt = ct.empty_outputs(x)
+        db = torch.empty(cols, device="cuda")
+        ct.fp8_dbias_cast_transpose(x, scalar(1.0), scalar(0.0), scalar(0.0), q, qt, db, ws, ct.E5M2)
+        outs.append(db.cpu().numpy().view(np.uint32))
+    assert np.array_equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("per_tensor_fmt", [False, True])
+def test_list_launch(per_tensor_fmt):
+    """One list launch of >= 2048 tiles: ragged entries, a one-tile-row entry,
+    and one entry that takes the general kernel (33 x 65)."""
+    shapes = [(4112, 1040), (2048, 2064), (16, 4096), (1024, 4096), (1040, 4096), (33, 65),
+              (4096, 4096), (144, 272)]
+    fmts = [ct.E4M3, ct.E5M2, ct.E5M2, ct.E4M3, ct.E5M2, ct.E4M3, ct.E4M3, ct.E5M2]
+    if not per_tensor_fmt:
+        fmts = [ct.E4M3] * len(shapes)
+    assert sum(_tiles(r, c) for r, c in shapes if r % 16 == 0 and c % 16 == 0) >= 2048
+    xs_cpu = [workloads.normal_bf16(r, c, 200.0, 1200 + i) for i, (r, c) in enumerate(shapes)]
+    n = len(xs_cpu)
+    scales = torch.tensor([1.0, 4.0, 0.5, 2.0, 8.0, 1.0, 0.25, 3.0], device="cuda")
+    amax = torch.full((n,), 0.5, device="cuda")
+    sinv = torch.zeros(n, device="cuda")
+    outs = [Guarded(x.numel()) for x in xs_cpu]
+    outs_t = [Guarded(x.numel()) for x in xs_cpu]
+    args = ([x.cuda() for x in xs_cpu], [scales[i:i + 1] for i in range(n)],
+            [amax[i:i + 1] for i in range(n)], [sinv[i:i + 1] for i in range(n)],
+            [o.t for o in outs], [o.t for o in outs_t])
+    if per_tensor_fmt:
+        ct.fp8_multi_cast_transpose_ex(*args, fmts)
+    else:
+        ct.fp8_multi_cast_transpose(*args, ct.E4M3)
+    torch.cuda.synchronize()
+    a, si = amax.cpu().numpy(), sinv.cpu().numpy()
+    for i, x in enumerate(xs_cpu):
+        r, c = x.shape
+        outs[i].check()
+        outs_t[i].check()
+        ref = oracle.cast_transpose(x, float(scales[i].item()), fmts[i], amax_in=0.5)
+        assert np.array_equal(outs[i].numpy().reshape(r, c), ref["q"]), i
+        assert np.array_equal(outs_t[i].numpy().reshape(c, r), ref["qt"]), i
+        assert f32_bits(a[i]) == f32_bits(ref["amax"]), i
+        assert f32_bits(si[i]) == f32_bits(ref["scale_inv"]), i
+
+
+def test_noop_and_graph_replay():
+    """Captured once; replay with flag 1 leaves every output as it was,
+    replay with flag 0 after a new input matches the oracle."""
+    rows, cols = RAGGED[0]
+    x_cpu = workloads.normal_bf16(rows, cols, 10.0, 3)
+    x = x_cpu.cuda()
+    q, qt = ct.empty_outputs(x)
+    db = torch.zeros(cols, device="cuda")
+    ws = torch.empty(ct.dbias_workspace_size(rows, cols), dtype=torch.uint8, device="cuda")
+    s, a, si = scalar(1.0), scalar(0.0), scalar(0.0)
+    flag = scalar(0.0)
+
+    def run():
+        ct.fp8_dbias_cast_transpose(x, s, a, si, q, qt, db, ws, ct.E4M3, noop_flag=flag)
+
+    run()   # first call outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    flag.fill_(1.0)
+    snap = [t.clone() for t in (q, qt, db, a, si)]
+    x.copy_(workloads.normal_bf16(rows, cols, 10.0, 4).cuda())
+    g.replay()
+    torch.cuda.synchronize()
+    for before, now in zip(snap, (q, qt, db, a, si)):
+        assert torch.equal(before.view(torch.uint8), now.view(torch.uint8))
+    x2 = workloads.normal_bf16(rows, cols, 10.0, 5)
+    x.copy_(x2.cuda())
+    flag.fill_(0.0)
+    a.fill_(0.0)
+    g.replay()
+    torch.cuda.synchronize()
+    ref = oracle.cast_transpose(x2, 1.0, ct.E4M3)
+    assert np.array_equal(q.cpu().numpy(), ref["q"])
+    assert np.array_equal(qt.cpu().numpy(), ref["qt"])
+    assert f32_bits(a.item()) == f32_bits(ref["amax"])
+    assert dbias_tolerance_ok(db.cpu().numpy(), oracle.dbias(x2), x2)
