@@ -547,7 +547,8 @@ def extra_kernels(dev, peaks) -> dict:
     ms = timed(lambda: ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3))
     b = 4 * x.numel() + 12
     res["cast_transpose 16384x12288 E4M3"] = {"us": round(ms * 1e3, 2), "GB/s": round(b / ms / 1e6, 1),
-                                               "frac": round(b / ms / 1e6 / peaks["hbm_gbs"], 4)}
+                                               "frac": round(b / ms / 1e6 / peaks["hbm_gbs"], 4),
+                                               "kernel": "direct_cast_transpose_kernel"}
     del x, q, qt
     # gradient 8192x12288, dbias + E5M2
     dy = workloads.gradient_matrix(dev)
@@ -558,7 +559,8 @@ def extra_kernels(dev, peaks) -> dict:
     b = 4 * dy.numel() + 4 * dy.shape[1] + 12
     res["dbias_cast_transpose 8192x12288 E5M2"] = {"us": round(ms * 1e3, 2),
                                                     "GB/s": round(b / ms / 1e6, 1),
-                                                    "frac": round(b / ms / 1e6 / peaks["hbm_gbs"], 4)}
+                                                    "frac": round(b / ms / 1e6 / peaks["hbm_gbs"], 4),
+                                                    "kernel": "direct_cast_transpose_kernel + dbias_finish_kernel"}
     del dy, q, qt
     # 48-tensor list, one multi launch
     xs = workloads.multi_list(dev)
@@ -571,15 +573,16 @@ def extra_kernels(dev, peaks) -> dict:
     b = sum(4 * x.numel() + 12 for x in xs)
     res["multi_cast_transpose 48 tensors E4M3"] = {"us": round(ms * 1e3, 2),
                                                     "GB/s": round(b / ms / 1e6, 1),
-                                                    "frac": round(b / ms / 1e6 / peaks["hbm_gbs"], 4)}
+                                                    "frac": round(b / ms / 1e6 / peaks["hbm_gbs"], 4),
+                                                    "kernel": "direct_cast_transpose_kernel (list)"}
     return res
 
 
 def profile_case(name: str) -> None:
     """Three launches of one kernel on one workload, for a profiler to
-    capture (ncu -k ... -s 2 -c 1): 'activation' (cast-transpose of the
-    16384x12288 activation, E4M3) or 'gradient' (dbias cast-transpose of the
-    8192x12288 gradient, E5M2)."""
+    capture (ncu -k regex:direct_cast -s 2 -c 1): 'activation' (cast-transpose
+    of the 16384x12288 activation, E4M3) or 'gradient' (dbias cast-transpose
+    of the 8192x12288 gradient, E5M2); both take the direct-load kernel."""
     import torch
 
     import cast_transpose_gb300 as ct
