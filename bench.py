@@ -575,21 +575,84 @@ def extra_kernels(dev, peaks) -> dict:
                                                     "GB/s": round(b / ms / 1e6, 1),
                                                     "frac": round(b / ms / 1e6 / peaks["hbm_gbs"], 4),
                                                     "kernel": "direct_cast_transpose_kernel (list)"}
+    # the 48-column update that follows the list (latency-bound: microseconds)
+    hist = torch.rand(16, n, device=dev)
+    rs = torch.ones(n, device=dev)
+    ms = timed(lambda: ct.fp8_amax_and_scale_update(hist, sc, rs, ct.E4M3, 0))
+    res["amax_and_scale_update n=48 L=16"] = {"us": round(ms * 1e3, 2),
+                                              "kernel": "scale_update_warp_kernel"}
+    del xs, outs, args
+    # the small 256x512 matrix (launch-bound: microseconds)
+    x = workloads.single_matrix(dev)
+    q, qt = ct.empty_outputs(x)
+    ms = timed(lambda: ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3), iters=10, per_graph=50)
+    res["cast_transpose 256x512 E4M3"] = {"us": round(ms * 1e3, 2), "kernel": "fast_cast_transpose_kernel"}
+    # activation: cast only (3 B/element), the gated launch with the flag set, FP8 byte transpose
+    x = workloads.activation_matrix(dev)
+    q, qt = ct.empty_outputs(x)
+    ms = timed(lambda: ct.fp8_cast(x, s1, a0, si0, q, ct.E4M3))
+    b = 3 * x.numel() + 12
+    res["cast 16384x12288 E4M3"] = {"us": round(ms * 1e3, 2), "GB/s": round(b / ms / 1e6, 1),
+                                    "frac": round(b / ms / 1e6 / peaks["hbm_gbs"], 4),
+                                    "kernel": "direct_cast_transpose_kernel (cast only)"}
+    flag = torch.ones(1, device=dev)
+    ms = timed(lambda: ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3, noop_flag=flag),
+               per_graph=50)
+    res["cast_transpose 16384x12288, noop flag set"] = {"us": round(ms * 1e3, 2)}
+    ms = timed(lambda: ct.fp8_transpose(q, qt))
+    b = 2 * x.numel()
+    res["transpose 16384x12288 FP8"] = {"us": round(ms * 1e3, 2), "GB/s": round(b / ms / 1e6, 1),
+                                        "frac": round(b / ms / 1e6 / peaks["hbm_gbs"], 4),
+                                        "kernel": "transpose_fast_kernel"}
     return res
 
 
 def profile_case(name: str) -> None:
-    """Three launches of one kernel on one workload, for a profiler to
-    capture (ncu -k regex:direct_cast -s 2 -c 1): 'activation' (cast-transpose
-    of the 16384x12288 activation, E4M3) or 'gradient' (dbias cast-transpose
-    of the 8192x12288 gradient, E5M2); both take the direct-load kernel."""
+    """Three launches of each kernel on one workload, for a profiler to
+    capture (ncu -k regex:<kernel> -s 2 -c 1):
+      'activation': cast-transpose of the 16384x12288 activation, E4M3;
+      'gradient':   dbias cast-transpose of the 8192x12288 gradient, E5M2
+                    (the direct-load kernel and the finish kernel);
+      'list':       a 12-tensor list (the four list shapes at half size), then
+                    three 48-column scale updates;
+      'cast':       cast only of the activation, then three FP8 transposes;
+      'general':    cast-transpose of a ragged 8191x12287 matrix."""
     import torch
 
     import cast_transpose_gb300 as ct
     from cast_transpose_gb300 import workloads
     dev = torch.device("cuda", 0)
     s1, a0, si0 = (torch.tensor([v], dtype=torch.float32, device=dev) for v in (1.0, 0.0, 0.0))
-    if name == "activation":
+    if name == "list":
+        # 12 tensors, 3 of each list shape at half size in both dimensions (1.2 GB in)
+        shapes = tuple((r // 2, c // 2) for r, c in workloads.MULTI_SHAPES)
+        xs = workloads.multi_list(dev, count=12, shapes=shapes, zero=(), tiny=())
+        outs = [ct.empty_outputs(x) for x in xs]
+        n = len(xs)
+        sc, am, si = (torch.ones(n, device=dev), torch.zeros(n, device=dev), torch.zeros(n, device=dev))
+        for _ in range(3):
+            ct.fp8_multi_cast_transpose(xs, [sc[i:i + 1] for i in range(n)],
+                                        [am[i:i + 1] for i in range(n)],
+                                        [si[i:i + 1] for i in range(n)], [o[0] for o in outs],
+                                        [o[1] for o in outs], ct.E4M3)
+        hist = torch.rand(16, 48, device=dev)
+        sc48, rs48 = torch.ones(48, device=dev), torch.ones(48, device=dev)
+        for _ in range(3):
+            ct.fp8_amax_and_scale_update(hist, sc48, rs48, ct.E4M3, 0)
+    elif name == "cast":
+        x = workloads.activation_matrix(dev)
+        q, qt = ct.empty_outputs(x)
+        for _ in range(3):
+            ct.fp8_cast(x, s1, a0, si0, q, ct.E4M3)
+        for _ in range(3):
+            ct.fp8_transpose(q, qt)
+    elif name == "general":
+        # ragged: neither dimension a multiple of 16 (the general kernel)
+        x = workloads.normal_bf16(8191, 12287, 1.0, 17, dev)
+        q, qt = ct.empty_outputs(x)
+        for _ in range(3):
+            ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3)
+    elif name == "activation":
         x = workloads.activation_matrix(dev)
         q, qt = ct.empty_outputs(x)
         for _ in range(3):
@@ -617,7 +680,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--extra", action=argparse.BooleanOptionalAction, default=True,
                     help="also time the dbias, multi-tensor and activation workloads")
-    ap.add_argument("--profile-case", choices=["activation", "gradient"], default=None,
+    ap.add_argument("--profile-case", choices=["activation", "gradient", "list", "cast", "general"],
+                    default=None,
                     help="only run 3 launches of one workload's kernel (for ncu) and exit")
     args = ap.parse_args()
     if args.profile_case:
