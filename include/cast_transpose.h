@@ -48,10 +48,12 @@
  *     argument returns an error code and launches nothing.  rows == 0 or
  *     cols == 0 returns CT_OK without a launch and writes nothing (its
  *     pointers are then not checked and may be NULL).  A failed launch returns
- *     CT_ERR_CUDA.  Any shape and alignment is accepted: dense shapes whose
- *     row lengths are multiples of 16 bytes and 16-byte-aligned buffers take
- *     the TMA-staged fast path, everything else a slower general kernel
- *     with identical results.
+ *     CT_ERR_CUDA.  Any shape and alignment is accepted.  Shapes with rows
+ *     and cols multiples of 16 and 16-byte-aligned buffers take a fast path:
+ *     a persistent TMA-staged kernel for launches under 2048 tiles of
+ *     128x128, a one-tile-per-CTA direct-load kernel from 2048 tiles on.
+ *     Everything else takes a slower general kernel.  All give identical
+ *     results.
  *   - Calls are thread-safe; the library keeps no per-call state.  The first
  *     call of an entry point on a device also sets its kernels' shared-memory
  *     limit (cudaFuncSetAttribute, once per device): make that first call
@@ -165,7 +167,7 @@ typedef struct {
 
 /*
  * fp8_multi_cast_transpose -- cast-transpose of a list of tensors, each with
- * its own scale, amax and scale-inverse, in one persistent launch ([B]: many
+ * its own scale, amax and scale-inverse, in one launch ([B]: many
  * FP8 weight workspaces are refreshed every step; one launch instead of one
  * per tensor keeps the host overhead flat).
  *
