@@ -1,7 +1,8 @@
 // ct_general.cu -- kernels for the cases the TMA path does not take, and the
 // small kernels around it (sm_103a):
 //   * general_cast_kernel: cast (+ transpose, + dbias partials) of a bf16
-//     matrix of ANY shape and alignment, 128x32 tiles, element-wise loads;
+//     matrix of ANY shape and alignment, 128x128 tiles, widest aligned
+//     loads and stores;
 //   * dbias_finish_kernel: db[j] = sum over 128-row tiles of the partials,
 //     compensated fp32, in a fixed order (deterministic);
 //   * scale_update_kernel: the delayed-scaling update of "[PyTorch] Refactor
@@ -19,83 +20,274 @@ namespace ct {
 namespace {
 
 // ---------------------------------------------------------------------------
-// General cast: tile = 128 rows x 32 columns, 256 threads; thread (c, g)
-// handles column c and rows g + 8*i, i = 0..15.
-constexpr int kGenCols = 32;
+// General cast: any shape, x 2-byte aligned, out and out_t 1-byte aligned.
+// Tile 128x128, 256 threads, the thread mapping of the direct-load kernel
+// (pass 1: 8-column chunk c of rows rg + 16*it; pass 2: 16-row x 4-column
+// byte blocks).  Loads and stores take the widest aligned form the address
+// allows, and never touch a byte outside the caller's buffers:
+//   * a row chunk (8 elements) is one 16-byte load when it is 16-byte
+//     aligned; otherwise the two aligned 16-byte blocks that cover it are
+//     loaded when both lie inside x, and the 8 elements are shifted out of
+//     them in registers; otherwise (the first and last blocks of x) the
+//     elements are loaded one by one;
+//   * elements past the end of the row read as zero (they belong to the next
+//     row) and are neither stored nor counted;
+//   * q chunks (8 bytes) and qT blocks (16 bytes) are stored with one vector
+//     store when aligned, else as aligned 4-byte words shifted across
+//     registers plus a 1- to 3-byte head and tail; chunks cut short by the
+//     matrix edge are stored byte by byte.
+namespace gen {
+
+// Word k + j of w[0..7], k in 0..3 (static indexing only).
+__device__ __forceinline__ uint32_t pick(const uint32_t (&w)[8], int j, int k) {
+    const uint32_t a = w[j], b = w[j + 1], c = w[j + 2], d = w[j + 3];
+    return k == 0 ? a : k == 1 ? b : k == 2 ? c : d;
+}
+
+// The 8 bf16 that start at element m (0..7) of the 16 held by lo, hi.
+__device__ __forceinline__ uint4 extract8(const uint4& lo, const uint4& hi, int m) {
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    const int k = m >> 1;
+    const uint32_t t0 = pick(w, 0, k), t1 = pick(w, 1, k), t2 = pick(w, 2, k),
+                   t3 = pick(w, 3, k), t4 = pick(w, 4, k);
+    if ((m & 1) == 0) return make_uint4(t0, t1, t2, t3);
+    // odd start: the high half of word k + j, then the low half of word k + j + 1
+    return make_uint4(__byte_perm(t0, t1, 0x5432), __byte_perm(t1, t2, 0x5432),
+                      __byte_perm(t2, t3, 0x5432), __byte_perm(t3, t4, 0x5432));
+}
+
+// Zero the elements n..7 of an 8-element chunk.
+__device__ __forceinline__ uint4 keep_first(uint4 v, int n) {
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        if (i >= n) w[i >> 1] &= (i & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ uint8_t byte_of(const uint32_t (&w)[4], int i) {
+    return static_cast<uint8_t>(w[i >> 2] >> (8 * (i & 3)));
+}
+
+// Store the K words d[0..K-1] (4K bytes) at dst, where h = dst & 3 is 1, 2
+// or 3: the 4 - h head bytes, K - 1 whole aligned words shifted across
+// registers (funnel shift by 8h bits), then the h tail bytes.
+template <int K>
+__device__ __forceinline__ void store_words_unaligned(uint8_t* dst, const uint32_t (&d)[K], int h) {
+    const uint32_t first = d[0], last = d[K - 1];
+    uint8_t* base = dst - h;   // 4-byte aligned
+#pragma unroll
+    for (int j = 1; j < K; ++j)
+        reinterpret_cast<uint32_t*>(base)[j] = __funnelshift_r(d[j - 1], d[j], 8 * (4 - h));
+    uint8_t* tail = base + 4 * K;
+    if (h == 1) {
+        dst[0] = static_cast<uint8_t>(first);
+        *reinterpret_cast<uint16_t*>(dst + 1) = static_cast<uint16_t>(first >> 8);
+        tail[0] = static_cast<uint8_t>(last >> 24);
+    } else if (h == 2) {
+        *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(first);
+        *reinterpret_cast<uint16_t*>(tail) = static_cast<uint16_t>(last >> 16);
+    } else {
+        dst[0] = static_cast<uint8_t>(first);
+        *reinterpret_cast<uint16_t*>(tail) = static_cast<uint16_t>(last >> 8);
+        tail[2] = static_cast<uint8_t>(last >> 24);
+    }
+}
+
+// Bytes 0..n-1 of the 16 in w to dst.
+__device__ __forceinline__ void store16(uint8_t* dst, const uint32_t (&w)[4], int n) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(dst);
+    if (n == 16) {
+        if ((a & 15) == 0) {
+            __stcs(reinterpret_cast<uint4*>(dst), make_uint4(w[0], w[1], w[2], w[3]));
+            return;
+        }
+        if ((a & 7) == 0) {
+            __stcs(reinterpret_cast<uint2*>(dst), make_uint2(w[0], w[1]));
+            __stcs(reinterpret_cast<uint2*>(dst + 8), make_uint2(w[2], w[3]));
+            return;
+        }
+        if ((a & 3) == 0) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) reinterpret_cast<uint32_t*>(dst)[j] = w[j];
+            return;
+        }
+        store_words_unaligned<4>(dst, w, static_cast<int>(a & 3));
+        return;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        if (i < n) dst[i] = byte_of(w, i);
+}
+
+// Bytes 0..n-1 of the 8 in q to dst.
+__device__ __forceinline__ void store8(uint8_t* dst, uint2 q, int n) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(dst);
+    if (n == 8) {
+        if ((a & 7) == 0) {
+            __stcs(reinterpret_cast<uint2*>(dst), q);
+            return;
+        }
+        if ((a & 3) == 0) {
+            reinterpret_cast<uint32_t*>(dst)[0] = q.x;
+            reinterpret_cast<uint32_t*>(dst)[1] = q.y;
+            return;
+        }
+        const uint32_t d[2] = {q.x, q.y};
+        store_words_unaligned<2>(dst, d, static_cast<int>(a & 3));
+        return;
+    }
+    const uint32_t w[4] = {q.x, q.y, 0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        if (i < n) dst[i] = byte_of(w, i);
+}
+
+}  // namespace gen
 
 template <int FMT, bool DBIAS>
-__global__ void __launch_bounds__(256) general_cast_kernel(GeneralArgs a) {
+__global__ void __launch_bounds__(256, 2) general_cast_kernel(GeneralArgs a) {
     dev::pdl_launch_dependents();
     dev::pdl_wait();
     if (a.noop != nullptr && *a.noop != 0.0f) return;
-    __shared__ uint8_t tileq[kTileRows][kGenCols + 4];
-    __shared__ float colsum[8][kGenCols];
-    __shared__ unsigned s_amax;
+    __shared__ __align__(16) uint8_t sq[kTileRows * kTileCols];
+    __shared__ __align__(16) float colsum[8 * kTileCols];
+    __shared__ unsigned s_amax[8];
 
-    const int64_t tiles_c = (a.cols + kGenCols - 1) / kGenCols;
-    const int64_t tiles = ((a.rows + kTileRows - 1) / kTileRows) * tiles_c;
-    const int tid = threadIdx.x;
-    const int c = tid & 31;
-    const int g = tid >> 5;
+    const int64_t rows = a.rows, cols = a.cols;
+    const int64_t tiles_c = (cols + kTileCols - 1) / kTileCols;
+    const int64_t tiles = ((rows + kTileRows - 1) / kTileRows) * tiles_c;
+    const uintptr_t xbeg = reinterpret_cast<uintptr_t>(a.x);
+    const uintptr_t xend = xbeg + 2 * uintptr_t(rows) * uintptr_t(cols);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int c = tid & 15, rg = tid >> 4;
+    const int b = lane & 7, w = warp * 4 + (lane >> 3);
     const float scale = *a.scale;
-    uint32_t amax = 0;
-    if (tid == 0) s_amax = 0;
-    __syncthreads();
 
     for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
         const int64_t rt = tile / tiles_c;
-        const int64_t row0 = rt * kTileRows;
-        const int64_t col0 = (tile - rt * tiles_c) * kGenCols;
-        const int64_t col = col0 + c;
-        float cs = 0.0f;
-        // all 16 loads of the thread first (memory-level parallelism), then
-        // the conversions and stores
-        uint16_t xv[16];
-        const bool col_ok = col < a.cols;
+        const int64_t row0 = rt * kTileRows, col0 = (tile - rt * tiles_c) * kTileCols;
+        const int64_t ccol = col0 + 8 * c;
+        const int nv = ccol >= cols ? 0 : (cols - ccol >= 8 ? 8 : static_cast<int>(cols - ccol));
+
+        // ---- loads: all issued before any use ----
+        uint4 lo[8], hi[8];
+        int mode[8];   // 0 none, 1 aligned, 2 two aligned blocks, 3 element-wise
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int64_t row = row0 + g + 8 * i;
-            xv[i] = (col_ok && row < a.rows) ? __ldg(a.x + row * a.cols + col) : uint16_t(0);
-        }
+        for (int it = 0; it < 8; ++it) {
+            const int64_t row = row0 + rg + 16 * it;
+            const int n = row < rows ? nv : 0;
+            const uint16_t* src = a.x + row * cols + ccol;
+            const uintptr_t ad = reinterpret_cast<uintptr_t>(src);
+            const uintptr_t b0 = ad & ~uintptr_t(15);
+            lo[it] = make_uint4(0u, 0u, 0u, 0u);
+            hi[it] = lo[it];
+            mode[it] = 0;
+            if (n > 0) {
+                if (b0 == ad && b0 + 16 <= xend) {
+                    lo[it] = __ldcs(reinterpret_cast<const uint4*>(b0));
+                    mode[it] = 1;
+                } else if (b0 >= xbeg && b0 + 32 <= xend) {
+                    lo[it] = __ldcs(reinterpret_cast<const uint4*>(b0));
+                    hi[it] = __ldcs(reinterpret_cast<const uint4*>(b0 + 16));
+                    mode[it] = 2;
+                } else {
+                    uint32_t e[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int r = g + 8 * i;
-            const int64_t row = row0 + r;
-            uint8_t code = 0;
-            if (col_ok && row < a.rows) {
-                const uint32_t bits = xv[i];
-                const uint32_t mag = (bits & 0x7FFFu) << 16;
-                amax = mag > amax ? mag : amax;
-                const float f = __uint_as_float(bits << 16);
-                if (DBIAS) cs += f;
-                code = static_cast<uint8_t>(dev::cvt_fp8x2<FMT>(__fmul_rn(f, scale), 0.0f));
-                if (a.out) a.out[row * a.cols + col] = code;
-            }
-            tileq[r][c] = code;
-        }
-        if (DBIAS) colsum[g][c] = cs;
-        __syncthreads();
-        if (a.out_t) {
-            // lanes run along rows of x, i.e. along a row of the transpose
-            const int r = tid & (kTileRows - 1);
-            const int64_t row = row0 + r;
-            for (int cc = tid >> 7; cc < kGenCols; cc += 2) {
-                const int64_t tc = col0 + cc;
-                if (row < a.rows && tc < a.cols) a.out_t[tc * a.rows + row] = tileq[r][cc];
+                    for (int i = 0; i < 8; ++i)
+                        if (i < n) e[i >> 1] |= uint32_t(__ldcs(src + i)) << (16 * (i & 1));
+                    lo[it] = make_uint4(e[0], e[1], e[2], e[3]);
+                    mode[it] = 3;
+                }
             }
         }
-        if (DBIAS && tid < kGenCols && col < a.cols) {
-            float s = colsum[0][tid];
-            for (int j = 1; j < 8; ++j) s += colsum[j][tid];
-            a.partial[rt * a.cols + col] = s;
+
+        // ---- pass 1: amax, column sums, cast, q and the FP8 copy ----
+        uint32_t amax_pair = 0;
+        float cs[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) cs[j] = 0.0f;
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+            const int r = rg + 16 * it;
+            const int64_t row = row0 + r;
+            const int n = row < rows ? nv : 0;
+            uint4 v = mode[it] == 2
+                          ? gen::extract8(lo[it], hi[it],
+                                          static_cast<int>((reinterpret_cast<uintptr_t>(
+                                                                a.x + row * cols + ccol) &
+                                                            15) >> 1))
+                          : lo[it];
+            if (n < 8) v = gen::keep_first(v, n);
+            amax_pair = dev::absmax_pair(amax_pair, v.x);
+            amax_pair = dev::absmax_pair(amax_pair, v.y);
+            amax_pair = dev::absmax_pair(amax_pair, v.z);
+            amax_pair = dev::absmax_pair(amax_pair, v.w);
+            if constexpr (DBIAS) {
+                cs[0] += dev::bf16_lo(v.x); cs[1] += dev::bf16_hi(v.x);
+                cs[2] += dev::bf16_lo(v.y); cs[3] += dev::bf16_hi(v.y);
+                cs[4] += dev::bf16_lo(v.z); cs[5] += dev::bf16_hi(v.z);
+                cs[6] += dev::bf16_lo(v.w); cs[7] += dev::bf16_hi(v.w);
+            }
+            const uint2 q8 = dev::cast8<FMT>(v, scale);
+            if (a.out != nullptr && n > 0) gen::store8(a.out + row * cols + ccol, q8, n);
+            *reinterpret_cast<uint2*>(sq + r * kTileCols + ((2 * c) ^ dev::swz(r)) * 4) = q8;
         }
-        if (tile == 0 && tid == 0) *a.scale_inv = __fdiv_rn(1.0f, scale);
+        const unsigned m = __reduce_max_sync(0xFFFFFFFFu, dev::pair_to_f32_bits(amax_pair));
+        if (lane == 0) s_amax[warp] = m;
+        if constexpr (DBIAS) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) cs[j] += __shfl_xor_sync(0xFFFFFFFFu, cs[j], 16);
+            if (lane < 16) {
+                float4* dst = reinterpret_cast<float4*>(colsum + warp * kTileCols + 8 * c);
+                dst[0] = make_float4(cs[0], cs[1], cs[2], cs[3]);
+                dst[1] = make_float4(cs[4], cs[5], cs[6], cs[7]);
+            }
+        }
         __syncthreads();
+
+        if (tid == 0) {
+            unsigned am = s_amax[0];
+#pragma unroll
+            for (int j = 1; j < 8; ++j) am = am > s_amax[j] ? am : s_amax[j];
+            if (am != 0) atomicMax(reinterpret_cast<unsigned*>(a.amax), am);
+            if (tile == 0) *a.scale_inv = __fdiv_rn(1.0f, scale);
+        }
+        if constexpr (DBIAS) {
+            if (tid < kTileCols && col0 + tid < cols) {
+                float sum = colsum[tid];
+#pragma unroll
+                for (int j = 1; j < 8; ++j) sum += colsum[j * kTileCols + tid];
+                a.partial[rt * cols + col0 + tid] = sum;
+            }
+        }
+
+        // ---- pass 2: transposed 16-row blocks of four columns ----
+        if (a.out_t != nullptr) {
+            const uint32_t* sq32 = reinterpret_cast<const uint32_t*>(sq);
+            uint32_t rw[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int r = 16 * b + j;
+                rw[j] = sq32[r * (kTileCols / 4) + (w ^ dev::swz(r))];
+            }
+            uint32_t o[4][4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+                dev::transpose4x4(rw[4 * g], rw[4 * g + 1], rw[4 * g + 2], rw[4 * g + 3], o[0][g],
+                                  o[1][g], o[2][g], o[3][g]);
+            const int64_t row = row0 + 16 * b;
+            const int nr = row >= rows ? 0 : (rows - row >= 16 ? 16 : static_cast<int>(rows - row));
+            if (nr > 0) {
+#pragma unroll
+                for (int kq = 0; kq < 4; ++kq) {
+                    const int64_t col = col0 + 4 * w + kq;
+                    if (col < cols) gen::store16(a.out_t + col * rows + row, o[kq], nr);
+                }
+            }
+        }
+        __syncthreads();   // sq, colsum and s_amax are reused by the next tile
     }
-    const unsigned m = __reduce_max_sync(0xFFFFFFFFu, amax);
-    if ((tid & 31) == 0 && m != 0) atomicMax(&s_amax, m);
-    __syncthreads();
-    if (tid == 0 && s_amax != 0) atomicMax(reinterpret_cast<unsigned*>(a.amax), s_amax);
 }
 
 // ---------------------------------------------------------------------------
@@ -288,8 +480,8 @@ unsigned grid_for(int64_t tiles, int64_t cap) {
 
 cudaError_t launch_general(const GeneralArgs& a, int fmt, cudaStream_t stream) {
     const int64_t tiles =
-        ((a.rows + kTileRows - 1) / kTileRows) * ((a.cols + kGenCols - 1) / kGenCols);
-    const dim3 grid(grid_for(tiles, 1 << 20)), block(256);
+        ((a.rows + kTileRows - 1) / kTileRows) * ((a.cols + kTileCols - 1) / kTileCols);
+    const dim3 grid(grid_for(tiles, int64_t(1) << 30)), block(256);
     const bool dbias = a.partial != nullptr;
     if (fmt == 0)
         return dbias ? launch_pdl(general_cast_kernel<0, true>, grid, block, 0, stream, a)
