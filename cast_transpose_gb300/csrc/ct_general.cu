@@ -9,7 +9,8 @@
 //     FP8 workspaces in linear modules" (Motivations: scale update kernel,
 //     infinite-scale case), one thread per tensor;
 //   * transpose kernels for FP8 bytes (the lazy transpose-cache fill of the
-//     same page), a 128x128-tile vectorised one and a general one.
+//     same page), a 128x128-tile vectorised one for aligned shapes and a
+//     128x128-tile one for any shape and alignment.
 #include "ct_device.cuh"
 #include "ct_internal.h"
 #include "ct_update.cuh"
@@ -62,6 +63,25 @@ __device__ __forceinline__ uint4 keep_first(uint4 v, int n) {
 #pragma unroll
     for (int i = 0; i < 8; ++i)
         if (i >= n) w[i >> 1] &= (i & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// The 16 bytes that start at byte m (0..15) of the 32 held by lo, hi.
+__device__ __forceinline__ uint4 extract16(const uint4& lo, const uint4& hi, int m) {
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    const int k = m >> 2, sh = 8 * (m & 3);
+    const uint32_t t0 = pick(w, 0, k), t1 = pick(w, 1, k), t2 = pick(w, 2, k),
+                   t3 = pick(w, 3, k), t4 = pick(w, 4, k);
+    return make_uint4(__funnelshift_r(t0, t1, sh), __funnelshift_r(t1, t2, sh),
+                      __funnelshift_r(t2, t3, sh), __funnelshift_r(t3, t4, sh));
+}
+
+// Zero the bytes n..15.
+__device__ __forceinline__ uint4 keep_first_bytes(uint4 v, int n) {
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        if (i >= n) w[i >> 2] &= ~(0xFFu << (8 * (i & 3)));
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
@@ -439,7 +459,12 @@ __global__ void __launch_bounds__(256) transpose_fast_kernel(const uint8_t* __re
     }
 }
 
-// General byte transpose: 32x32 tiles, any shape and alignment.
+// General byte transpose: any shape, in and out at any byte.  128x128
+// tiles with the fast kernel's layout; each 16-byte row chunk is one aligned
+// load, else the two aligned blocks covering it (both inside `in`) shifted in
+// registers, else byte loads (first and last blocks of `in` only); bytes past
+// the row end are zeroed.  The transposed 16-byte blocks are stored with
+// gen::store16.
 __global__ void __launch_bounds__(256) transpose_general_kernel(const uint8_t* __restrict__ in,
                                                                 int64_t rows, int64_t cols,
                                                                 uint8_t* __restrict__ out,
@@ -447,25 +472,83 @@ __global__ void __launch_bounds__(256) transpose_general_kernel(const uint8_t* _
     dev::pdl_launch_dependents();
     dev::pdl_wait();
     if (noop != nullptr && *noop != 0.0f) return;
-    __shared__ uint8_t tile[32][33];
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    const int64_t tiles_c = (cols + 31) / 32;
-    const int64_t tiles = ((rows + 31) / 32) * tiles_c;
+    __shared__ __align__(16) uint32_t tile[kTileRows * (kTileCols / 4)];
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const uintptr_t ibeg = reinterpret_cast<uintptr_t>(in);
+    const uintptr_t iend = ibeg + uintptr_t(rows) * uintptr_t(cols);
+    const int64_t tiles_c = (cols + kTileCols - 1) / kTileCols;
+    const int64_t tiles = ((rows + kTileRows - 1) / kTileRows) * tiles_c;
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
         const int64_t rt = t / tiles_c;
-        const int64_t row0 = rt * 32, col0 = (t - rt * tiles_c) * 32;
-        uint8_t v[4];
+        const int64_t row0 = rt * kTileRows, col0 = (t - rt * tiles_c) * kTileCols;
+        // chunk ch (16 bytes) of row r; 1024 chunks, 4 per thread
+        uint4 lo[4], hi[4];
+        int mode[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int64_t row = row0 + ty + 8 * i, col = col0 + tx;
-            v[i] = (row < rows && col < cols) ? __ldg(in + row * cols + col) : uint8_t(0);
+            const int idx = tid + 256 * i;
+            const int r = idx >> 3, ch = idx & 7;
+            const int64_t row = row0 + r, col = col0 + 16 * ch;
+            const int n = (row >= rows || col >= cols) ? 0
+                          : (cols - col >= 16 ? 16 : static_cast<int>(cols - col));
+            const uint8_t* src = in + row * cols + col;
+            const uintptr_t ad = reinterpret_cast<uintptr_t>(src);
+            const uintptr_t b0 = ad & ~uintptr_t(15);
+            lo[i] = make_uint4(0u, 0u, 0u, 0u);
+            hi[i] = lo[i];
+            mode[i] = 0;
+            if (n > 0) {
+                if (b0 == ad && b0 + 16 <= iend) {
+                    lo[i] = __ldg(reinterpret_cast<const uint4*>(b0));
+                    mode[i] = 1;
+                } else if (b0 >= ibeg && b0 + 32 <= iend) {
+                    lo[i] = __ldg(reinterpret_cast<const uint4*>(b0));
+                    hi[i] = __ldg(reinterpret_cast<const uint4*>(b0 + 16));
+                    mode[i] = 2;
+                } else {
+                    uint32_t e[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (j < n) e[j >> 2] |= uint32_t(__ldg(src + j)) << (8 * (j & 3));
+                    lo[i] = make_uint4(e[0], e[1], e[2], e[3]);
+                    mode[i] = 3;
+                }
+            }
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) tile[ty + 8 * i][tx] = v[i];
+        for (int i = 0; i < 4; ++i) {
+            const int idx = tid + 256 * i;
+            const int r = idx >> 3, ch = idx & 7;
+            const int64_t row = row0 + r, col = col0 + 16 * ch;
+            const int n = (row >= rows || col >= cols) ? 0
+                          : (cols - col >= 16 ? 16 : static_cast<int>(cols - col));
+            uint4 v = lo[i];
+            if (mode[i] == 2) {
+                const int m = static_cast<int>(reinterpret_cast<uintptr_t>(in + row * cols + col) & 15);
+                v = gen::extract16(lo[i], hi[i], m);
+            }
+            if (n < 16) v = gen::keep_first_bytes(v, n);
+            *reinterpret_cast<uint4*>(&tile[r * 32 + ((4 * ch) ^ (4 * (r >> 4)))]) = v;
+        }
         __syncthreads();
-        for (int cc = ty; cc < 32; cc += 8) {
-            const int64_t col = col0 + cc, row = row0 + tx;
-            if (row < rows && col < cols) out[col * rows + row] = tile[tx][cc];
+        const int b = lane & 7, w = warp * 4 + (lane >> 3);
+        uint32_t rw[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) rw[j] = tile[(16 * b + j) * 32 + (w ^ (4 * b))];
+        uint32_t o[4][4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+            dev::transpose4x4(rw[4 * g], rw[4 * g + 1], rw[4 * g + 2], rw[4 * g + 3], o[0][g],
+                              o[1][g], o[2][g], o[3][g]);
+        const int64_t row = row0 + 16 * b;
+        const int nr = row >= rows ? 0 : (rows - row >= 16 ? 16 : static_cast<int>(rows - row));
+        if (nr > 0) {
+#pragma unroll
+            for (int kq = 0; kq < 4; ++kq) {
+                const int64_t col = col0 + 4 * w + kq;
+                if (col < cols) gen::store16(out + col * rows + row, o[kq], nr);
+            }
         }
         __syncthreads();
     }
@@ -518,8 +601,8 @@ cudaError_t launch_transpose(const uint8_t* in, int64_t rows, int64_t cols, uint
         return launch_pdl(transpose_fast_kernel, dim3(grid_for(tiles, 4096)), dim3(256), 0, stream,
                           in, rows, cols, out, noop);
     }
-    const int64_t tiles = ((rows + 31) / 32) * ((cols + 31) / 32);
-    return launch_pdl(transpose_general_kernel, dim3(grid_for(tiles, 1 << 20)), dim3(256), 0,
+    const int64_t tiles = ((rows + 127) / 128) * ((cols + 127) / 128);
+    return launch_pdl(transpose_general_kernel, dim3(grid_for(tiles, int64_t(1) << 30)), dim3(256), 0,
                       stream, in, rows, cols, out, noop);
 }
 

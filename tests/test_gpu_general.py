@@ -103,3 +103,20 @@ def test_single_row_and_column_misaligned():
         x_cpu = workloads.normal_bf16(*shape, 1.0, shape[0] * 7 + shape[1])
         got = cast_transpose_gpu(_shifted(x_cpu, 1), 1.0, ct.E4M3, out_offset=3)
         assert_same_cast(got, oracle.cast_transpose(x_cpu, 1.0, ct.E4M3))
+
+
+@pytest.mark.parametrize("in_shift", [0, 1, 3, 7, 8, 13])
+@pytest.mark.parametrize("shape", [(131, 257), (256, 200), (1031, 2053)])
+def test_fp8_transpose_general(shape, in_shift):
+    """fp8_transpose on shapes / offsets outside the 16-byte fast path: every
+    byte offset class of the input, outputs at odd offsets."""
+    rows, cols = shape
+    g = torch.Generator().manual_seed(rows + 7 * cols + in_shift)
+    q_cpu = torch.randint(0, 256, (rows, cols), dtype=torch.uint8, generator=g)
+    big = torch.empty(rows * cols + 32, dtype=torch.uint8, device="cuda")
+    big[in_shift:in_shift + rows * cols] = q_cpu.reshape(-1).cuda()
+    out = Guarded(rows * cols, offset=(in_shift * 5) % 16)
+    ct.fp8_transpose(big[in_shift:in_shift + rows * cols].view(rows, cols), out.t)
+    torch.cuda.synchronize()
+    out.check()
+    assert np.array_equal(out.numpy().reshape(cols, rows), oracle.fp8_transpose(q_cpu.numpy()))
