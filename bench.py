@@ -604,6 +604,16 @@ def extra_kernels(dev, peaks) -> dict:
     res["transpose 16384x12288 FP8"] = {"us": round(ms * 1e3, 2), "GB/s": round(b / ms / 1e6, 1),
                                         "frac": round(b / ms / 1e6 / peaks["hbm_gbs"], 4),
                                         "kernel": "transpose_fast_kernel"}
+    del x, q, qt
+    # a ragged shape (odd rows and cols): the general kernel
+    x = workloads.normal_bf16(8191, 12287, 1.0, 17, dev)
+    q, qt = ct.empty_outputs(x)
+    ms = timed(lambda: ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3))
+    b = 4 * x.numel() + 12
+    res["cast_transpose 8191x12287 E4M3 (ragged)"] = {"us": round(ms * 1e3, 2),
+                                                      "GB/s": round(b / ms / 1e6, 1),
+                                                      "frac": round(b / ms / 1e6 / peaks["hbm_gbs"], 4),
+                                                      "kernel": "general_cast_kernel"}
     return res
 
 
@@ -616,7 +626,8 @@ def profile_case(name: str) -> None:
       'list':       a 12-tensor list (the four list shapes at half size), then
                     three 48-column scale updates;
       'cast':       cast only of the activation, then three FP8 transposes;
-      'general':    cast-transpose of a ragged 8191x12287 matrix."""
+      'general':    cast-transpose of a ragged 8191x12287 matrix, then three
+                    FP8 transposes of its q (the general kernels)."""
     import torch
 
     import cast_transpose_gb300 as ct
@@ -652,6 +663,8 @@ def profile_case(name: str) -> None:
         q, qt = ct.empty_outputs(x)
         for _ in range(3):
             ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3)
+        for _ in range(3):
+            ct.fp8_transpose(q, qt)
     elif name == "activation":
         x = workloads.activation_matrix(dev)
         q, qt = ct.empty_outputs(x)
