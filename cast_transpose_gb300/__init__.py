@@ -29,6 +29,7 @@ import torch
 
 E4M3 = 0
 E5M2 = 1
+X_READY = 1          # fp8_cast_transpose_ex flag CT_X_READY
 FP8_MAX = {E4M3: 448.0, E5M2: 57344.0}
 TORCH_FP8 = {E4M3: torch.float8_e4m3fn, E5M2: torch.float8_e5m2}
 
@@ -70,6 +71,8 @@ def lib() -> ctypes.CDLL:
             L.ct_status_string.restype = c.c_char_p
             L.ct_status_string.argtypes = [i32]
             L.fp8_cast_transpose.argtypes = [vp, i64, i64, vp, vp, vp, vp, vp, i32, vp, vp]
+            L.fp8_cast_transpose_ex.argtypes = [vp, i64, i64, vp, vp, vp, vp, vp, i32, vp,
+                                                c.c_uint, vp]
             L.fp8_cast.argtypes = [vp, i64, i64, vp, vp, vp, vp, i32, vp, vp]
             L.fp8_dbias_cast_transpose.argtypes = [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp,
                                                    c.c_size_t, i32, vp, vp]
@@ -84,7 +87,8 @@ def lib() -> ctypes.CDLL:
             L.ct_device_error.argtypes = [c.POINTER(c.c_uint), i32]
             L.ct_selftest_bounded_wait.argtypes = [c.c_uint, vp]
             L.ct_selftest_bounded_wait.restype = i32
-            for name in ("fp8_cast_transpose", "fp8_cast", "fp8_dbias_cast_transpose",
+            for name in ("fp8_cast_transpose", "fp8_cast_transpose_ex", "fp8_cast",
+                         "fp8_dbias_cast_transpose",
                          "fp8_multi_cast_transpose", "fp8_multi_cast_transpose_ex",
                          "fp8_amax_and_scale_update", "fp8_amax_and_scale_update_ex",
                          "fp8_transpose", "ct_device_error"):
@@ -139,14 +143,19 @@ def _rc(x: torch.Tensor):
 
 
 def fp8_cast_transpose(x, scale, amax, scale_inv, out, out_t, fmt=E4M3, noop_flag=None,
-                       stream=None) -> None:
+                       stream=None, x_ready=False) -> None:
+    """x_ready=True calls fp8_cast_transpose_ex with CT_X_READY: the caller
+    promises that no kernel still running when this call starts writes x."""
     rows, cols = _rc(x)
     n = rows * cols
-    _check(lib().fp8_cast_transpose(
-        _dev(x, "x", torch.bfloat16), rows, cols, _dev(scale, "scale", torch.float32, 1),
-        _dev(amax, "amax", torch.float32, 1), _dev(scale_inv, "scale_inv", torch.float32, 1),
-        _dev(out, "out", _U8, n), _dev(out_t, "out_t", _U8, n), fmt, _opt(noop_flag, "noop_flag"),
-        _stream(stream)))
+    args = (_dev(x, "x", torch.bfloat16), rows, cols, _dev(scale, "scale", torch.float32, 1),
+            _dev(amax, "amax", torch.float32, 1), _dev(scale_inv, "scale_inv", torch.float32, 1),
+            _dev(out, "out", _U8, n), _dev(out_t, "out_t", _U8, n), fmt,
+            _opt(noop_flag, "noop_flag"))
+    if x_ready:
+        _check(lib().fp8_cast_transpose_ex(*args, X_READY, _stream(stream)))
+    else:
+        _check(lib().fp8_cast_transpose(*args, _stream(stream)))
 
 
 def fp8_cast(x, scale, amax, scale_inv, out, fmt=E4M3, noop_flag=None, stream=None) -> None:

@@ -132,7 +132,8 @@ void fill_tensor(FastTensor& t, const void* out, const void* out_t, const float*
 // row on the general path).
 int cast_impl(const void* x, int64_t rows, int64_t cols, const float* scale, float* amax,
               float* scale_inv, void* out, void* out_t, float* partial, int fmt,
-              const float* noop, cudaStream_t stream, int64_t* runs_out = nullptr) {
+              const float* noop, cudaStream_t stream, int64_t* runs_out = nullptr,
+              bool x_ready = false) {
     const int64_t R = (rows + ct::kTileRows - 1) / ct::kTileRows;
     if (fast_eligible(x, rows, cols, out, out_t)) {
         const int64_t tiles = R * ((cols + ct::kTileCols - 1) / ct::kTileCols);
@@ -156,6 +157,7 @@ int cast_impl(const void* x, int64_t rows, int64_t cols, const float* scale, flo
         p.total_tiles = p.t[0].tile_end;
         p.noop = noop;
         p.partial = partial;
+        p.x_ready = x_ready ? 1 : 0;
         if (runs_out) *runs_out = ct::dbias_units(R, R < ct::kDbiasBand ? R : ct::kDbiasBand).bands;
         return cuda_status(ct::launch_fast(p, fmt, partial != nullptr, out_t ? 0 : 1, stream));
     }
@@ -203,6 +205,17 @@ int fp8_cast_transpose(const void* x, int64_t rows, int64_t cols, const float* s
     if (rows == 0 || cols == 0) return CT_OK;
     return cast_impl(x, rows, cols, scale, amax, scale_inv, out, out_t, nullptr, fmt, noop_flag,
                      static_cast<cudaStream_t>(stream));
+}
+
+int fp8_cast_transpose_ex(const void* x, int64_t rows, int64_t cols, const float* scale,
+                          float* amax, float* scale_inv, void* out, void* out_t, int fmt,
+                          const float* noop_flag, unsigned flags, void* stream) {
+    if (flags & ~static_cast<unsigned>(CT_X_READY)) return CT_ERR_ARG;
+    const int st = check_cast(x, rows, cols, scale, amax, scale_inv, out, out_t, true, fmt);
+    if (st != CT_OK) return st;
+    if (rows == 0 || cols == 0) return CT_OK;
+    return cast_impl(x, rows, cols, scale, amax, scale_inv, out, out_t, nullptr, fmt, noop_flag,
+                     static_cast<cudaStream_t>(stream), nullptr, (flags & CT_X_READY) != 0);
 }
 
 int fp8_cast(const void* x, int64_t rows, int64_t cols, const float* scale, float* amax,

@@ -165,6 +165,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// 2-D tiled bulk tensor prefetch into L2: no shared memory and no completion
+// signal, only a hint.  L2 is where every write of the GPU lands, so a line
+// prefetched before its last write is simply updated by it: a prefetch can
+// never make a later read see stale data.  Same coordinate rules as the load.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // ---- 4x4 byte transpose ------------------------------------------------------
 // r0..r3 hold rows 0..3 of a 4x4 byte block (byte k = column k); on return
 // c0..c3 hold its columns (byte i = row i).

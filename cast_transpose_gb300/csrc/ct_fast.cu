@@ -195,9 +195,9 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
         const uint64_t policy = WRITE_T ? dev::policy_evict_first() : dev::policy_evict_normal();
         int icur = 0;
         uint32_t issued = 0;
-        auto issue = [&](uint32_t kk) {
-            const int s = static_cast<int>(kk % STAGES);
-            StageInfo inf;
+        // Where tile kk of this CTA comes from; `ic` is the list entry of the
+        // previous call's tile (tiles only move forward through the list).
+        auto locate = [&](uint32_t kk, int& ic, StageInfo& inf) {
             if constexpr (DBIAS) {
                 int64_t m, off, h;
                 if (int64_t(kk) < dsch.F * dsch.H) {
@@ -220,9 +220,9 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
                 inf.seg = static_cast<int32_t>(band);
             } else {
                 const int64_t tile = int64_t(first) + int64_t(kk) * G;
-                while (tile >= p.t[icur].tile_end) ++icur;
-                const FastTensor& T = p.t[icur];
-                inf.tensor = icur;
+                while (tile >= p.t[ic].tile_end) ++ic;
+                const FastTensor& T = p.t[ic];
+                inf.tensor = ic;
                 inf.last = (kk + 1 == my_tiles) || (tile + G >= T.tile_end);
                 tile_coords(static_cast<uint32_t>(tile - T.tile_begin),
                             static_cast<uint32_t>(T.tile_rows), static_cast<uint32_t>(T.tile_cols),
@@ -230,18 +230,35 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
                 inf.seg_end = 0;
                 inf.seg = 0;
             }
+        };
+        auto issue = [&](uint32_t kk) {
+            const int s = static_cast<int>(kk % STAGES);
+            StageInfo inf;
+            locate(kk, icur, inf);
             info[s] = inf;
             dev::mbar_arrive_expect_tx(&full[s], kStageBytes);
             dev::tma_load_2d(stages + s * kStageBytes, &p.map[icur], inf.ct * kTileCols,
                              inf.rt * kTileRows, &full[s], policy);
         };
-        // The first STAGES tile loads go out before the dependency wait: x is
-        // bf16 input, which no kernel of this library writes, so it can be
-        // fetched while the preceding kernel in the stream (when it is one of
-        // this library's, launched as a programmatic dependent) still runs.
-        for (; issued < my_tiles && issued < STAGES; ++issued) issue(issued);
+        // The preceding kernel in the stream may still run until the
+        // dependency wait returns, and it may be the one writing x: by default
+        // the first STAGES tiles are only prefetched into L2 before the wait
+        // (a hint, which cannot leave stale data behind) and loaded after it.
+        // When the caller promises that no running kernel writes x (x_ready),
+        // they are loaded before the wait, overlapping the preceding kernel.
+        if (p.x_ready) {
+            for (; issued < my_tiles && issued < STAGES; ++issued) issue(issued);
+        } else {
+            int ic = 0;
+            for (uint32_t kk = 0; kk < my_tiles && kk < STAGES; ++kk) {
+                StageInfo inf;
+                locate(kk, ic, inf);
+                dev::tma_prefetch_l2_2d(&p.map[ic], inf.ct * kTileCols, inf.rt * kTileRows);
+            }
+        }
         dev::pdl_wait();
         bool stop = p.noop != nullptr && *p.noop != 0.0f;
+        for (; !stop && issued < my_tiles && issued < STAGES; ++issued) issue(issued);
         for (; !stop && issued < my_tiles; ++issued) {
             const uint32_t kk = issued;
             if (!dev::mbar_wait_bounded(&empty[kk % STAGES], ((kk / STAGES) - 1) & 1u, s_abort)) {

@@ -44,6 +44,8 @@ struct FastParams {
     int64_t total_tiles;
     const float* noop;     // nullable device flag
     float* partial;        // dbias partials [ceil(rows/128), cols], or null
+    int x_ready;           // caller's promise: no kernel still running writes x
+                           // (the first tiles may be loaded before the dependency wait)
 };
 
 // Arguments of the general (any shape / alignment) kernels.

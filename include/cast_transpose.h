@@ -59,12 +59,11 @@
  *     limit (cudaFuncSetAttribute, once per device): make that first call
  *     outside stream capture, as one makes a warm-up call before capturing.
  *   - Kernels are launched as programmatic dependents of the previous kernel
- *     in the stream: a cast kernel may start fetching its bf16 input while
- *     the library's preceding kernel on that stream is still finishing.
- *     Every other read, and every write, waits for that kernel to complete.
- *     The library never writes bf16 data, so this is invisible unless an
- *     output buffer of the immediately preceding call is reinterpreted as
- *     this call's bf16 input, which is not allowed.
+ *     in the stream: they may be scheduled while it still runs, and read or
+ *     write nothing before it has completed.  A cast kernel may only ask for
+ *     its first tiles of x to be prefetched into L2 meanwhile, a hint that
+ *     cannot return stale data.  fp8_cast_transpose_ex with CT_X_READY lets
+ *     it load them, under that flag's precondition.
  */
 #ifndef CAST_TRANSPOSE_GB300_H
 #define CAST_TRANSPOSE_GB300_H
@@ -123,6 +122,29 @@ int fp8_cast_transpose(const void* x, int64_t rows, int64_t cols,
                        const float* scale, float* amax, float* scale_inv,
                        void* out, void* out_t, int fmt,
                        const float* noop_flag, void* stream);
+
+/* Flags of fp8_cast_transpose_ex. */
+typedef enum {
+    /* The caller promises that no kernel that may still be running when this
+     * call's kernel starts writes x: x was produced by a copy or a kernel the
+     * stream has already waited for, and the kernel just before this call in
+     * the stream does not write it (for example, it is this library's scale
+     * update, which writes only fp32 scalars).  The call may then load its
+     * first tiles of x before the preceding kernel completes.  Without the
+     * flag nothing of x is read until that kernel has completed. */
+    CT_X_READY = 1u
+} ct_cast_flags;
+
+/*
+ * fp8_cast_transpose_ex -- fp8_cast_transpose with `flags`, a bitwise OR of
+ * ct_cast_flags values.  The pages have no counterpart: the flag only moves
+ * the moment x is first read (see CT_X_READY), never what is computed.
+ * Errors: as fp8_cast_transpose, plus CT_ERR_ARG for an unknown flag bit.
+ */
+int fp8_cast_transpose_ex(const void* x, int64_t rows, int64_t cols,
+                          const float* scale, float* amax, float* scale_inv,
+                          void* out, void* out_t, int fmt,
+                          const float* noop_flag, unsigned flags, void* stream);
 
 /*
  * fp8_dbias_cast_transpose -- [A] DbiasCastTranspose.backward:

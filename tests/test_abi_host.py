@@ -26,7 +26,7 @@ def L():
 
 def test_exports_every_declared_function(L):
     names = ct.header_functions()
-    expected = {"fp8_cast_transpose", "fp8_dbias_cast_transpose",
+    expected = {"fp8_cast_transpose", "fp8_cast_transpose_ex", "fp8_dbias_cast_transpose",
                 "fp8_dbias_cast_transpose_workspace_size", "fp8_multi_cast_transpose",
                 "fp8_amax_and_scale_update", "fp8_transpose", "fp8_cast", "ct_status_string",
                 "ct_device_error"}
@@ -61,6 +61,21 @@ def test_cast_transpose_rejects(L):
     assert _ct(L, qt=Q + 100) == CT_ERR_ALIAS          # outputs overlap
     assert _ct(L, sinv=S) == CT_ERR_ALIAS              # scale_inv over scale
     assert _ct(L, amax=SI) == CT_ERR_ALIAS
+
+
+def test_cast_transpose_ex_rejects(L):
+    def ex(flags, **kw):
+        a = dict(x=X, rows=64, cols=64, scale=S, amax=A, sinv=SI, q=Q, qt=QT, fmt=0)
+        a.update(kw)
+        return L.fp8_cast_transpose_ex(a["x"], a["rows"], a["cols"], a["scale"], a["amax"],
+                                       a["sinv"], a["q"], a["qt"], a["fmt"], None, flags, None)
+    assert ex(2) == CT_ERR_ARG                      # unknown flag bit
+    assert ex(0x80000000) == CT_ERR_ARG
+    assert ex(ct.X_READY, x=None) == CT_ERR_NULL    # the same checks as fp8_cast_transpose
+    assert ex(ct.X_READY, fmt=3) == CT_ERR_FORMAT
+    assert ex(ct.X_READY, q=X) == CT_ERR_ALIAS
+    assert ex(ct.X_READY, rows=0) == CT_OK
+    assert ex(0, cols=0) == CT_OK
 
 
 def test_empty_shapes_are_ok_without_launch(L):

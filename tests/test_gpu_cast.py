@@ -172,12 +172,15 @@ def test_more_than_2_to_31_elements():
     assert si.item() == 0.5
 
 
-def test_weight_step_as_benchmarked():
+@pytest.mark.parametrize("x_ready", [True, False])
+def test_weight_step_as_benchmarked(x_ready):
     """The benchmark's launch configuration: the 4096x4096 step (x * 2^k for
     k = -4..3, each cast followed by the update) captured once in a CUDA
     graph and replayed, with programmatic dependent launch between the 16
     kernels; one eager warm-up step, then two replays.  Every output of the
-    last replay and the history/scale state match the oracle."""
+    last replay and the history/scale state match the oracle.  The benchmark
+    passes CT_X_READY (x_ready=True): each cast follows the scale update,
+    which writes no bf16 data."""
     L = 16
     base = workloads.weight_matrix("cuda")
     xs = [workloads.weight_rescaled(base, k) for k in workloads.WEIGHT_EXPONENTS]
@@ -188,7 +191,8 @@ def test_weight_step_as_benchmarked():
 
     def step():
         for k, x in enumerate(xs):
-            ct.fp8_cast_transpose(x, scale, hist[0], tsi[k:k + 1], outs[k][0], outs[k][1], ct.E4M3)
+            ct.fp8_cast_transpose(x, scale, hist[0], tsi[k:k + 1], outs[k][0], outs[k][1], ct.E4M3,
+                                  x_ready=x_ready)
             ct.fp8_amax_and_scale_update(hist, scale, rsi, ct.E4M3, 0)
 
     side = torch.cuda.Stream()
@@ -218,3 +222,32 @@ def test_weight_step_as_benchmarked():
             h, s, si = oracle.amax_and_scale_update(h, s, si, ct.E4M3, 0)
     assert np.array_equal(hist.cpu().numpy().view(np.uint32), h.view(np.uint32))
     assert f32_bits(scale.item()) == f32_bits(s[0]) and f32_bits(rsi.item()) == f32_bits(si[0])
+
+
+def test_input_written_by_the_preceding_kernel():
+    """Without CT_X_READY a cast reads nothing of x before the kernel before
+    it in the stream has completed.  Here that kernel (a torch in-place sign
+    flip) writes x itself, 24 times in a row, eagerly and in a replayed graph:
+    every cast must see the flipped values."""
+    x_cpu = workloads.normal_bf16(4096, 4096, 1.0, 31)
+    ref_pos = oracle.cast_transpose(x_cpu, 1.0, ct.E4M3)
+    ref_neg = oracle.cast_transpose(-x_cpu, 1.0, ct.E4M3)
+    want = [(torch.from_numpy(r["q"]).cuda(), torch.from_numpy(r["qt"]).cuda())
+            for r in (ref_pos, ref_neg)]
+    x = x_cpu.cuda()
+    q, qt = ct.empty_outputs(x)
+    s, a, si = scalar(1.0), scalar(0.0), scalar(0.0)
+    for i in range(24):
+        x.neg_()                                    # x := -x, the kernel just before the cast
+        ct.fp8_cast_transpose(x, s, a, si, q, qt, ct.E4M3)
+        sign = (i + 1) % 2                          # 1: x = -x_cpu
+        assert torch.equal(q, want[sign][0]) and torch.equal(qt, want[sign][1]), i
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        x.neg_()
+        ct.fp8_cast_transpose(x, s, a, si, q, qt, ct.E4M3)
+    for i in range(6):
+        g.replay()
+        torch.cuda.synchronize()
+        sign = (24 + i + 1) % 2
+        assert torch.equal(q, want[sign][0]) and torch.equal(qt, want[sign][1]), i

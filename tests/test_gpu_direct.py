@@ -176,3 +176,51 @@ def test_noop_and_graph_replay():
     assert np.array_equal(qt.cpu().numpy(), ref["qt"])
     assert f32_bits(a.item()) == f32_bits(ref["amax"])
     assert dbias_tolerance_ok(db.cpu().numpy(), oracle.dbias(x2), x2)
+
+
+@pytest.mark.parametrize("tile_rows", [2047, 2048])
+def test_dispatch_boundary(tile_rows):
+    """2047 tiles (persistent TMA kernel) and 2048 tiles (direct kernel) of a
+    one-tile-wide matrix, dbias included: the same bits either side."""
+    rows, cols = 128 * tile_rows, 128
+    x_cpu = workloads.gradient_matrix("cpu", rows, cols, std=1e-2, outlier_fraction=1e-4)
+    n = rows * cols
+    q, qt = Guarded(n), Guarded(n)
+    db = Guarded(cols, dtype=torch.float32)
+    ws = torch.empty(ct.dbias_workspace_size(rows, cols), dtype=torch.uint8, device="cuda")
+    s, a, si = scalar(2.0), scalar(0.0), scalar(0.0)
+    ct.fp8_dbias_cast_transpose(x_cpu.cuda(), s, a, si, q.t, qt.t, db.t, ws, ct.E4M3)
+    torch.cuda.synchronize()
+    for g in (q, qt, db):
+        g.check()
+    ref = oracle.cast_transpose(x_cpu, 2.0, ct.E4M3)
+    assert np.array_equal(q.numpy().reshape(rows, cols), ref["q"])
+    assert np.array_equal(qt.numpy().reshape(cols, rows), ref["qt"])
+    assert f32_bits(a.item()) == f32_bits(ref["amax"])
+    assert dbias_tolerance_ok(db.numpy(), oracle.dbias(x_cpu), x_cpu)
+
+
+def test_long_list_direct_then_persistent():
+    """70 tensors: the first launch of 64 (2048 tiles) takes the direct
+    kernel, the remaining 6 the persistent one."""
+    shapes = [(512, 1024)] * 64 + [(256, 384), (16, 4096), (128, 128), (640, 1040), (48, 48),
+                                   (1024, 16)]
+    xs_cpu = [workloads.normal_bf16(r, c, 3.0, 5000 + i) for i, (r, c) in enumerate(shapes)]
+    assert sum(_tiles(r, c) for r, c in shapes[:64]) == 2048
+    n = len(xs_cpu)
+    scales = torch.tensor([float(1 + i % 5) for i in range(n)], device="cuda")
+    amax = torch.zeros(n, device="cuda")
+    sinv = torch.zeros(n, device="cuda")
+    outs = [torch.empty(x.numel(), dtype=torch.uint8, device="cuda") for x in xs_cpu]
+    outs_t = [torch.empty(x.numel(), dtype=torch.uint8, device="cuda") for x in xs_cpu]
+    ct.fp8_multi_cast_transpose([x.cuda() for x in xs_cpu], [scales[i:i + 1] for i in range(n)],
+                                [amax[i:i + 1] for i in range(n)], [sinv[i:i + 1] for i in range(n)],
+                                outs, outs_t, ct.E5M2)
+    torch.cuda.synchronize()
+    a = amax.cpu().numpy()
+    for i, x in enumerate(xs_cpu):
+        r, c = x.shape
+        ref = oracle.cast_transpose(x, float(1 + i % 5), ct.E5M2)
+        assert np.array_equal(outs[i].cpu().numpy().reshape(r, c), ref["q"]), i
+        assert np.array_equal(outs_t[i].cpu().numpy().reshape(c, r), ref["qt"]), i
+        assert f32_bits(a[i]) == f32_bits(ref["amax"]), i
