@@ -1,6 +1,8 @@
 // ct_api.cu -- the C ABI of include/cast_transpose.h: host-side argument
-// checks, TMA descriptor encoding and dispatch between the TMA-staged path
-// and the general path.  No device memory is allocated here, no stream or
+// checks, TMA descriptor encoding and dispatch between the persistent
+// TMA-staged kernel (fast shapes, under kDirectMinTiles tiles), the
+// direct-load kernel (fast shapes, from kDirectMinTiles tiles on) and the
+// general kernel (every other shape and alignment).  No device memory is allocated here, no stream or
 // device is synchronised, and no device memory is read, so every call can be
 // captured in a CUDA graph.
 #include "../../include/cast_transpose.h"
@@ -129,7 +131,7 @@ void fill_tensor(FastTensor& t, const void* out, const void* out_t, const float*
 
 // `runs_out` (dbias only): the number of partial rows the launched kernel
 // writes per column (one per band of tile rows on the TMA path, one per tile
-// row on the general path).
+// row on the direct and general paths).  `x_ready`: CT_X_READY (TMA path).
 int cast_impl(const void* x, int64_t rows, int64_t cols, const float* scale, float* amax,
               float* scale_inv, void* out, void* out_t, float* partial, int fmt,
               const float* noop, cudaStream_t stream, int64_t* runs_out = nullptr,
