@@ -51,7 +51,8 @@ def _brute_force_encode(p: np.ndarray, fmt: int, maxcode: int, maxval: float):
     grid = _torch_decode(torch.float8_e4m3fn if fmt == oracle.E4M3 else torch.float8_e5m2)
     grid = grid[: maxcode + 1].astype(np.float64)
     assert np.all(np.diff(grid) > 0)
-    a = np.abs(p.astype(np.float64))
+    with np.errstate(invalid="ignore"):      # signalling-NaN patterns among the probes
+        a = np.abs(p.astype(np.float64))
     hi = np.clip(np.searchsorted(grid, a, side="left"), 0, maxcode)
     lo = np.clip(hi - 1, 0, maxcode)
     d_lo = np.abs(a - grid[lo])
