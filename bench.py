@@ -621,6 +621,10 @@ def extra_kernels(dev, peaks) -> dict:
     q, qt = ct.empty_outputs(x)
     ms = timed(lambda: ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3), iters=10, per_graph=50)
     res["cast_transpose 256x512 E4M3"] = {"us": round(ms * 1e3, 2), "kernel": "fast_cast_transpose_kernel"}
+    ms = timed(lambda: ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3, x_ready=True), iters=10,
+               per_graph=50)
+    res["cast_transpose 256x512 E4M3, CT_X_READY"] = {"us": round(ms * 1e3, 2),
+                                                      "kernel": "fast_cast_transpose_kernel"}
     # activation: cast only (3 B/element), the gated launch with the flag set, FP8 byte transpose
     x = workloads.activation_matrix(dev)
     q, qt = ct.empty_outputs(x)
