@@ -67,6 +67,7 @@ def lib() -> ctypes.CDLL:
             L.oracle_amax.argtypes = [c.c_void_p, c.c_int64, c.c_void_p]
             L.oracle_dbias.argtypes = [c.c_void_p, c.c_int64, c.c_int64, c.c_void_p]
             L.oracle_fp8_transpose.argtypes = [c.c_void_p, c.c_int64, c.c_int64, c.c_void_p]
+            L.oracle_f32_to_bf16_array.argtypes = [c.c_void_p, c.c_int64, c.c_void_p]
             L.oracle_amax_and_scale_update.argtypes = [c.c_void_p, c.c_void_p, c.c_void_p,
                                                        c.c_int, c.c_int, c.c_int, c.c_int]
             L.oracle_amax_and_scale_update_algo.argtypes = [c.c_void_p, c.c_void_p, c.c_void_p,
@@ -139,6 +140,19 @@ def dbias(x) -> np.ndarray:
     db = np.empty(cols, dtype=np.float32)
     lib().oracle_dbias(_ptr(x), rows, cols, _ptr(db))
     return db
+
+
+def f32_to_bf16(f) -> np.ndarray:
+    """bf16 bit patterns (uint16) of fp32 values, round to nearest even."""
+    f = np.ascontiguousarray(f, dtype=np.float32)
+    out = np.empty(f.shape, dtype=np.uint16)
+    lib().oracle_f32_to_bf16_array(_ptr(f), f.size, _ptr(out))
+    return out
+
+
+def dbias_bf16(x) -> np.ndarray:
+    """db as bf16 bit patterns: the fp32 column sum of dbias(), rounded to bf16."""
+    return f32_to_bf16(dbias(x))
 
 
 def fp8_transpose(q: np.ndarray) -> np.ndarray:

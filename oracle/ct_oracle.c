@@ -210,6 +210,38 @@ void oracle_dbias(const uint16_t* x, int64_t rows, int64_t cols, float* db)
     }
 }
 
+/* fp32 -> bf16 by the IEEE rule, written out: the two bf16 values that
+ * bracket |f| are its truncation to 8 significand bits and the next one up
+ * (past the largest finite bf16, that next one stands for 2^128, i.e. the
+ * overflow to Inf); the nearer one wins, a tie goes to the even significand.
+ * The distances are exact in double.  NaN gives the canonical quiet NaN
+ * 0x7FFF (reading: the pages never round a NaN db; the choice follows the
+ * hardware conversion's canonical NaN).  Used for a bf16 db: the fp32 column
+ * sum rounded once more, to bf16. */
+uint16_t oracle_f32_to_bf16(float f)
+{
+    const uint32_t u = f32_bits(f);
+    const uint32_t sign = u & 0x80000000u, mag = u & 0x7FFFFFFFu;
+    if (mag > 0x7F800000u) return 0x7FFF;                       /* NaN */
+    if (mag == 0x7F800000u) return (uint16_t)((sign | mag) >> 16); /* +-Inf */
+    const uint32_t lo = mag & 0xFFFF0000u;                       /* truncation */
+    const uint32_t hi = lo + 0x10000u;                           /* next bf16 up */
+    const double a = (double)f32_from_bits(mag);
+    const double vlo = (double)f32_from_bits(lo);
+    const double vhi = hi == 0x7F800000u ? ldexp(1.0, 128) : (double)f32_from_bits(hi);
+    const double dlo = a - vlo, dhi = vhi - a;
+    uint32_t pick;
+    if (dlo < dhi) pick = lo;
+    else if (dhi < dlo) pick = hi;
+    else pick = ((lo >> 16) & 1u) ? hi : lo;                     /* tie: even */
+    return (uint16_t)((sign | pick) >> 16);
+}
+
+void oracle_f32_to_bf16_array(const float* f, int64_t count, uint16_t* out)
+{
+    for (int64_t i = 0; i < count; ++i) out[i] = oracle_f32_to_bf16(f[i]);
+}
+
 /* Byte transpose of an FP8 matrix: out[j*rows + i] = in[i*cols + j]
  * (the transpose-cache fill, "[PyTorch] Refactor FP8 workspaces in linear
  * modules", the lazy transpose caching bullet). */
