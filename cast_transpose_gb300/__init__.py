@@ -30,6 +30,7 @@ import torch
 E4M3 = 0
 E5M2 = 1
 X_READY = 1          # fp8_cast_transpose_ex flag CT_X_READY
+DBIAS_FP32, DBIAS_BF16 = 0, 1   # fp8_dbias_cast_transpose_ex db element types
 FP8_MAX = {E4M3: 448.0, E5M2: 57344.0}
 TORCH_FP8 = {E4M3: torch.float8_e4m3fn, E5M2: torch.float8_e5m2}
 
@@ -76,6 +77,8 @@ def lib() -> ctypes.CDLL:
             L.fp8_cast.argtypes = [vp, i64, i64, vp, vp, vp, vp, i32, vp, vp]
             L.fp8_dbias_cast_transpose.argtypes = [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp,
                                                    c.c_size_t, i32, vp, vp]
+            L.fp8_dbias_cast_transpose_ex.argtypes = [vp, i64, i64, vp, vp, vp, vp, vp, vp, i32,
+                                                      vp, c.c_size_t, i32, vp, vp]
             L.fp8_dbias_cast_transpose_workspace_size.restype = c.c_size_t
             L.fp8_dbias_cast_transpose_workspace_size.argtypes = [i64, i64]
             L.fp8_multi_cast_transpose.argtypes = [vp, i32, i32, vp, vp]
@@ -88,7 +91,7 @@ def lib() -> ctypes.CDLL:
             L.ct_selftest_bounded_wait.argtypes = [c.c_uint, vp]
             L.ct_selftest_bounded_wait.restype = i32
             for name in ("fp8_cast_transpose", "fp8_cast_transpose_ex", "fp8_cast",
-                         "fp8_dbias_cast_transpose",
+                         "fp8_dbias_cast_transpose", "fp8_dbias_cast_transpose_ex",
                          "fp8_multi_cast_transpose", "fp8_multi_cast_transpose_ex",
                          "fp8_amax_and_scale_update", "fp8_amax_and_scale_update_ex",
                          "fp8_transpose", "ct_device_error"):
@@ -172,15 +175,20 @@ def dbias_workspace_size(rows: int, cols: int) -> int:
 
 def fp8_dbias_cast_transpose(dy, scale, amax, scale_inv, out, out_t, dbias, workspace,
                              fmt=E5M2, noop_flag=None, stream=None) -> None:
+    """dbias: fp32 or bf16 [cols]; a bf16 dbias calls fp8_dbias_cast_transpose_ex
+    with CT_DBIAS_BF16."""
     rows, cols = _rc(dy)
     n = rows * cols
     ws = _dev(workspace, "workspace", torch.uint8)
-    _check(lib().fp8_dbias_cast_transpose(
-        _dev(dy, "dy", torch.bfloat16), rows, cols, _dev(scale, "scale", torch.float32, 1),
-        _dev(amax, "amax", torch.float32, 1), _dev(scale_inv, "scale_inv", torch.float32, 1),
-        _dev(out, "out", _U8, n), _dev(out_t, "out_t", _U8, n),
-        _dev(dbias, "dbias", torch.float32, cols), ws, workspace.numel(), fmt,
-        _opt(noop_flag, "noop_flag"), _stream(stream)))
+    db = _dev(dbias, "dbias", (torch.float32, torch.bfloat16), cols)
+    head = (_dev(dy, "dy", torch.bfloat16), rows, cols, _dev(scale, "scale", torch.float32, 1),
+            _dev(amax, "amax", torch.float32, 1), _dev(scale_inv, "scale_inv", torch.float32, 1),
+            _dev(out, "out", _U8, n), _dev(out_t, "out_t", _U8, n), db)
+    tail = (ws, workspace.numel(), fmt, _opt(noop_flag, "noop_flag"), _stream(stream))
+    if dbias.dtype == torch.bfloat16:
+        _check(lib().fp8_dbias_cast_transpose_ex(*head, DBIAS_BF16, *tail))
+    else:
+        _check(lib().fp8_dbias_cast_transpose(*head, *tail))
 
 
 def _descs(xs, scales, amaxes, scale_invs, outs, outs_t):

@@ -239,16 +239,28 @@ int fp8_dbias_cast_transpose(const void* dy, int64_t rows, int64_t cols, const f
                              float* amax, float* scale_inv, void* out, void* out_t,
                              float* dbias, void* workspace, size_t workspace_bytes, int fmt,
                              const float* noop_flag, void* stream) {
+    return fp8_dbias_cast_transpose_ex(dy, rows, cols, scale, amax, scale_inv, out, out_t, dbias,
+                                       CT_DBIAS_FP32, workspace, workspace_bytes, fmt, noop_flag,
+                                       stream);
+}
+
+int fp8_dbias_cast_transpose_ex(const void* dy, int64_t rows, int64_t cols, const float* scale,
+                                float* amax, float* scale_inv, void* out, void* out_t,
+                                void* dbias, int dbias_dtype, void* workspace,
+                                size_t workspace_bytes, int fmt, const float* noop_flag,
+                                void* stream) {
+    if (dbias_dtype != CT_DBIAS_FP32 && dbias_dtype != CT_DBIAS_BF16) return CT_ERR_ARG;
     int st = check_cast(dy, rows, cols, scale, amax, scale_inv, out, out_t, true, fmt);
     if (st != CT_OK) return st;
     if (rows == 0 || cols == 0) return CT_OK;
     if (!dbias) return CT_ERR_NULL;
-    if (!aligned(dbias, 4)) return CT_ERR_ALIGN;
+    const int64_t db_elem = dbias_dtype == CT_DBIAS_BF16 ? 2 : 4;
+    if (!aligned(dbias, uintptr_t(db_elem))) return CT_ERR_ALIGN;
     const size_t need = fp8_dbias_cast_transpose_workspace_size(rows, cols);
     if (!workspace || workspace_bytes < need) return CT_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return CT_ERR_ALIGN;
     const int64_t n = rows * cols;
-    const Range rdb = range_of(dbias, 4 * cols), rws = range_of(workspace, int64_t(need));
+    const Range rdb = range_of(dbias, db_elem * cols), rws = range_of(workspace, int64_t(need));
     const Range others[6] = {range_of(dy, 2 * n), range_of(out, n), range_of(out_t, n),
                              range_of(scale, 4), range_of(amax, 4), range_of(scale_inv, 4)};
     if (overlap(rdb, rws)) return CT_ERR_ALIAS;
@@ -260,7 +272,8 @@ int fp8_dbias_cast_transpose(const void* dy, int64_t rows, int64_t cols, const f
     st = cast_impl(dy, rows, cols, scale, amax, scale_inv, out, out_t, partial, fmt, noop_flag, s,
                    &runs);
     if (st != CT_OK) return st;
-    return cuda_status(ct::launch_dbias_finish(partial, runs, cols, dbias, noop_flag, s));
+    return cuda_status(ct::launch_dbias_finish(partial, runs, cols, dbias,
+                                               dbias_dtype == CT_DBIAS_BF16, noop_flag, s));
 }
 
 namespace {

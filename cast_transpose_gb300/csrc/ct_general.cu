@@ -4,7 +4,8 @@
 //     matrix of ANY shape and alignment, 128x128 tiles, widest aligned
 //     loads and stores;
 //   * dbias_finish_kernel: db[j] = sum over 128-row tiles of the partials,
-//     compensated fp32, in a fixed order (deterministic);
+//     compensated fp32, in a fixed order (deterministic), stored as fp32 or
+//     rounded to bf16;
 //   * scale_update_kernel: the delayed-scaling update of "[PyTorch] Refactor
 //     FP8 workspaces in linear modules" (Motivations: scale update kernel,
 //     infinite-scale case), one thread per tensor;
@@ -14,6 +15,8 @@
 #include "ct_device.cuh"
 #include "ct_internal.h"
 #include "ct_update.cuh"
+
+#include <cuda_bf16.h>
 
 #include <cmath>
 
@@ -333,19 +336,23 @@ __global__ void __launch_bounds__(256, CT_GEN_MINB) general_cast_kernel(GeneralA
 // compensated (Kahan) fp32: the error stays within a few fp32 ulps of the sum
 // of magnitudes for any number of row tiles, without fp64 arithmetic, which
 // runs at a small fraction of the fp32 rate on this GPU.
+// Once the sum is not finite (an Inf or NaN in the column) the compensation
+// is dropped, so the sum keeps the plain IEEE result (Inf, or NaN for
+// Inf - Inf and NaN inputs) instead of the Inf - Inf of the correction term.
 struct Kahan {
     float sum = 0.0f, comp = 0.0f;
     __device__ __forceinline__ void add(float v) {
         const float y = __fsub_rn(v, comp);
         const float t = __fadd_rn(sum, y);
-        comp = __fsub_rn(__fsub_rn(t, sum), y);
+        comp = isfinite(t) ? __fsub_rn(__fsub_rn(t, sum), y) : 0.0f;
         sum = t;
     }
 };
 
+template <bool BF16_OUT>
 __global__ void __launch_bounds__(256) dbias_finish_kernel(const float* __restrict__ partial,
                                                            int64_t runs, int64_t cols,
-                                                           float* __restrict__ db,
+                                                           void* __restrict__ db,
                                                            const float* noop) {
     dev::pdl_launch_dependents();
     dev::pdl_wait();
@@ -370,7 +377,10 @@ __global__ void __launch_bounds__(256) dbias_finish_kernel(const float* __restri
                 total.add(part[q][c]);
                 total.add(-comp[q][c]);
             }
-            db[j] = total.sum;
+            if constexpr (BF16_OUT)
+                static_cast<uint16_t*>(db)[j] = __bfloat16_as_ushort(__float2bfloat16_rn(total.sum));
+            else
+                static_cast<float*>(db)[j] = total.sum;
         }
         __syncthreads();
     }
@@ -588,10 +598,14 @@ cudaError_t launch_general(const GeneralArgs& a, int fmt, cudaStream_t stream) {
                  : launch_pdl(general_cast_kernel<1, false>, grid, block, 0, stream, a);
 }
 
-cudaError_t launch_dbias_finish(const float* partial, int64_t runs, int64_t cols, float* dbias,
-                                const float* noop, cudaStream_t stream) {
+cudaError_t launch_dbias_finish(const float* partial, int64_t runs, int64_t cols, void* dbias,
+                                bool db_bf16, const float* noop, cudaStream_t stream) {
     const dim3 grid(grid_for((cols + 31) / 32, 1 << 16)), block(256);
-    return launch_pdl(dbias_finish_kernel, grid, block, 0, stream, partial, runs, cols, dbias, noop);
+    if (db_bf16)
+        return launch_pdl(dbias_finish_kernel<true>, grid, block, 0, stream, partial, runs, cols,
+                          dbias, noop);
+    return launch_pdl(dbias_finish_kernel<false>, grid, block, 0, stream, partial, runs, cols,
+                      dbias, noop);
 }
 
 cudaError_t launch_scale_update(float* hist, float* scale, float* scale_inv, int hist_len,

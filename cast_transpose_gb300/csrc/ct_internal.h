@@ -150,9 +150,10 @@ __host__ __device__ __forceinline__ DbiasUnits dbias_units(int64_t R, int64_t H)
 #endif
 constexpr int64_t kDbiasBand = CT_DBIAS_BAND;
 
-// Dbias finish: db[j] = sum of the `runs` partial rows (compensated fp32).
-cudaError_t launch_dbias_finish(const float* partial, int64_t runs, int64_t cols, float* dbias,
-                                const float* noop, cudaStream_t stream);
+// Dbias finish: db[j] = sum of the `runs` partial rows (compensated fp32),
+// stored as fp32, or (db_bf16) rounded to bf16, nearest even.
+cudaError_t launch_dbias_finish(const float* partial, int64_t runs, int64_t cols, void* dbias,
+                                bool db_bf16, const float* noop, cudaStream_t stream);
 
 // Scale update of `count` columns of a [hist_len, stride] history (scale and
 // scale_inv indexed like the columns).

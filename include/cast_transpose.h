@@ -174,6 +174,32 @@ int fp8_dbias_cast_transpose(const void* dy, int64_t rows, int64_t cols,
  * (0 when rows or cols is 0 or negative). */
 size_t fp8_dbias_cast_transpose_workspace_size(int64_t rows, int64_t cols);
 
+/* Element type of fp8_dbias_cast_transpose_ex's db output. */
+typedef enum {
+    CT_DBIAS_FP32 = 0,   /* fp32, as fp8_dbias_cast_transpose                   */
+    CT_DBIAS_BF16 = 1    /* the same fp32 column sum, rounded to bf16 (nearest
+                            even; NaN -> 0x7FFF), e.g. for a bf16 bias         */
+} ct_dbias_dtype;
+
+/*
+ * fp8_dbias_cast_transpose_ex -- fp8_dbias_cast_transpose with the db element
+ * type as an argument ([A] DbiasCastTranspose.backward: db is the gradient of
+ * the bias, which a bf16 model keeps in bf16).
+ *
+ *   dbias        [cols] output of type dbias_dtype, 4-byte (fp32) or 2-byte
+ *                (bf16) aligned; must not overlap the other buffers
+ *   dbias_dtype  CT_DBIAS_FP32 or CT_DBIAS_BF16
+ *   (every other argument as in fp8_dbias_cast_transpose)
+ *
+ * Errors: as fp8_dbias_cast_transpose, plus CT_ERR_ARG for an unknown
+ * dbias_dtype.
+ */
+int fp8_dbias_cast_transpose_ex(const void* dy, int64_t rows, int64_t cols,
+                                const float* scale, float* amax, float* scale_inv,
+                                void* out, void* out_t, void* dbias, int dbias_dtype,
+                                void* workspace, size_t workspace_bytes, int fmt,
+                                const float* noop_flag, void* stream);
+
 /* One entry of a tensor list (host memory; the pointers inside are device
  * pointers with the meaning they have in fp8_cast_transpose). */
 typedef struct {

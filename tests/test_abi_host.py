@@ -27,6 +27,7 @@ def L():
 def test_exports_every_declared_function(L):
     names = ct.header_functions()
     expected = {"fp8_cast_transpose", "fp8_cast_transpose_ex", "fp8_dbias_cast_transpose",
+                "fp8_dbias_cast_transpose_ex",
                 "fp8_dbias_cast_transpose_workspace_size", "fp8_multi_cast_transpose",
                 "fp8_amax_and_scale_update", "fp8_transpose", "fp8_cast", "ct_status_string",
                 "ct_device_error"}
@@ -102,6 +103,17 @@ def test_dbias_rejects(L):
     assert call(db=X) == CT_ERR_ALIAS
     assert call(ws=Q) == CT_ERR_ALIAS
     assert call(rows=0) == CT_OK
+
+    def ex(dtype, db=DB, ws=WS):
+        return L.fp8_dbias_cast_transpose_ex(X, 300, 70, S, A, SI, Q, QT, db, dtype, ws, need, 1,
+                                             None, None)
+    assert ex(2) == CT_ERR_ARG                      # unknown db element type
+    assert ex(-1) == CT_ERR_ARG
+    assert ex(ct.DBIAS_BF16, db=DB + 1) == CT_ERR_ALIGN
+    assert ex(ct.DBIAS_FP32, db=DB + 2) == CT_ERR_ALIGN
+    assert ex(ct.DBIAS_BF16, db=None) == CT_ERR_NULL
+    assert ex(ct.DBIAS_BF16, ws=None) == CT_ERR_WORKSPACE
+    assert ex(ct.DBIAS_BF16, db=X + 2) == CT_ERR_ALIAS
 
 
 def test_update_rejects(L):

@@ -86,3 +86,82 @@ def test_gradient_8192x12288_two_steps():
                                            ct.E5M2, 0)
     got2 = run_dbias(dy, float(s[0]), ct.E5M2)
     check(got2, x_cpu, float(s[0]), ct.E5M2)
+
+
+def _bf16_to_f32(bits):
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def dbias_bf16_tolerance_ok(db_bits, x_cpu) -> bool:
+    """bf16 db: the fp32 bound widened by the bf16 rounding (half a bf16 ulp,
+    at most 2^-8 of the value): |db - ref| <= T + 2^-8 (|ref| + T), with
+    T = 1e-5 * sum_i |dy[i, j]| + 1e-6 and ref the oracle's double sum."""
+    ref = oracle.dbias(x_cpu).astype(np.float64)
+    t = 1e-5 * x_cpu.double().abs().sum(dim=0).numpy() + 1e-6
+    got = _bf16_to_f32(db_bits).astype(np.float64)
+    return bool(np.all(np.abs(got - ref) <= t + 2.0 ** -8 * (np.abs(ref) + t)))
+
+
+@pytest.mark.parametrize("shape,x_shift", [((2048, 272), 0), ((4112, 8208), 0), ((1000, 771), 1),
+                                           ((131072, 256), 0)])
+def test_bf16_db(shape, x_shift):
+    """CT_DBIAS_BF16 on the TMA, direct and general paths: FP8 outputs
+    bit-exact, db within the bf16 bound, and equal to the oracle's bf16 db
+    on at least 99% of the columns (the rest sit on a bf16 rounding edge)."""
+    rows, cols = shape
+    x_cpu = workloads.gradient_matrix("cpu", rows, cols, std=1e-3, outlier_fraction=1e-3)
+    big = torch.empty(rows * cols + 8, dtype=torch.bfloat16, device="cuda")
+    big[x_shift:x_shift + rows * cols] = x_cpu.reshape(-1).cuda()
+    dy = big[x_shift:x_shift + rows * cols].view(rows, cols)
+    n = rows * cols
+    q, qt = Guarded(n), Guarded(n)
+    db = Guarded(cols, dtype=torch.bfloat16)
+    ws = torch.empty(ct.dbias_workspace_size(rows, cols), dtype=torch.uint8, device="cuda")
+    ws.fill_(0x7F)
+    s, a, si = scalar(2.0), scalar(0.0), scalar(0.0)
+    ct.fp8_dbias_cast_transpose(dy, s, a, si, q.t, qt.t, db.t, ws, ct.E5M2)
+    torch.cuda.synchronize()
+    for g in (q, qt, db):
+        g.check()
+    ref = oracle.cast_transpose(x_cpu, 2.0, ct.E5M2)
+    assert np.array_equal(q.numpy().reshape(rows, cols), ref["q"])
+    assert np.array_equal(qt.numpy().reshape(cols, rows), ref["qt"])
+    assert f32_bits(a.item()) == f32_bits(ref["amax"])
+    bits = db.t.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert dbias_bf16_tolerance_ok(bits, x_cpu)
+    assert np.mean(bits == oracle.dbias_bf16(x_cpu)) >= 0.99
+
+
+@pytest.mark.parametrize("db_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("shape", [(512, 256), (4112, 8208), (300, 70)])
+def test_db_of_inf_and_nan_columns(shape, db_dtype):
+    """Columns holding +Inf, -Inf, NaN, and +Inf with -Inf: db is +Inf, -Inf,
+    NaN and NaN (the IEEE sums the oracle gives); the other columns are
+    unaffected."""
+    rows, cols = shape
+    x = workloads.gradient_matrix("cpu", rows, cols, std=1e-2, outlier_fraction=0.0).float()
+    x[rows // 3, 3] = float("inf")
+    x[rows - 1, 5] = float("-inf")
+    x[0, 7] = float("nan")
+    x[1, 9] = float("inf")
+    x[rows - 2, 9] = float("-inf")
+    x_cpu = x.to(torch.bfloat16)
+    ref = oracle.dbias(x_cpu)
+    assert np.isposinf(ref[3]) and np.isneginf(ref[5]) and np.isnan(ref[7]) and np.isnan(ref[9])
+    q, qt = ct.empty_outputs(x_cpu.cuda())
+    db = torch.empty(cols, dtype=db_dtype, device="cuda")
+    ws = torch.empty(ct.dbias_workspace_size(rows, cols), dtype=torch.uint8, device="cuda")
+    ct.fp8_dbias_cast_transpose(x_cpu.cuda(), scalar(1.0), scalar(0.0), scalar(0.0), q, qt, db, ws,
+                                ct.E5M2)
+    torch.cuda.synchronize()
+    got = db.float().cpu().numpy()
+    assert np.isposinf(got[3]) and np.isneginf(got[5]) and np.isnan(got[7]) and np.isnan(got[9])
+    rest = np.ones(cols, bool)
+    rest[[3, 5, 7, 9]] = False
+    if db_dtype == torch.float32:
+        assert np.all(np.abs(got[rest].astype(np.float64) - ref[rest]) <=
+                      1e-5 * x_cpu.double().abs().sum(0).numpy()[rest] + 1e-6)
+    else:
+        bits = db.view(torch.int16).cpu().numpy().view(np.uint16)
+        assert bits[7] == 0x7FFF and bits[9] == 0x7FFF      # canonical NaN (the oracle's reading)
+        assert np.array_equal(bits[[3, 5]], oracle.dbias_bf16(x_cpu)[[3, 5]])
