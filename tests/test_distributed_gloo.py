@@ -3,6 +3,9 @@
 * amax_allreduce: ranks hold different amaxes (their shards of a tensor);
   after the MAX all-reduce every rank has the elementwise maximum, and the
   oracle's scale update then yields identical scales on every rank.
+* dbias_allreduce: each rank holds the db of its rows of dy (the oracle's
+  column sums of its shard); after the SUM all-reduce both ranks hold the
+  same bits, within the dbias tolerance of the column sums of the whole dy.
 * bench.py's max-over-ranks timing reduction, with gloo standing in for
   NCCL: the slowest rank's time is what both ranks see.
 """
@@ -73,6 +76,34 @@ def test_amax_allreduce_gloo_world2():
     for r in (0, 1):
         assert np.array_equal(out[r]["reduced"], want)
     assert np.array_equal(out[0]["scale"].view(np.uint32), out[1]["scale"].view(np.uint32))
+
+
+def _dbias_case(rank, world):
+    import oracle
+    from cast_transpose_gb300 import workloads
+    from cast_transpose_gb300.distributed import dbias_allreduce
+    dy = workloads.gradient_matrix("cpu", 512, 300, std=1e-2, outlier_fraction=1e-3)
+    shard = dy[rank * 256:(rank + 1) * 256]
+    db = torch.from_numpy(oracle.dbias(shard).copy())
+    dbias_allreduce(db)
+    return {"db": db.numpy().copy()}
+
+
+def test_dbias_allreduce_gloo_world2():
+    out = _run(_dbias_case)
+    import oracle
+    from cast_transpose_gb300 import workloads
+    dy = workloads.gradient_matrix("cpu", 512, 300, std=1e-2, outlier_fraction=1e-3)
+    ref = oracle.dbias(dy).astype(np.float64)
+    tol = 1e-5 * dy.double().abs().sum(0).numpy() + 1e-6
+    assert np.array_equal(out[0]["db"].view(np.uint32), out[1]["db"].view(np.uint32))
+    assert np.all(np.abs(out[0]["db"].astype(np.float64) - ref) <= tol)
+
+
+def test_dbias_allreduce_rejects_bf16():
+    from cast_transpose_gb300.distributed import dbias_allreduce
+    with pytest.raises(TypeError):
+        dbias_allreduce(torch.zeros(4, dtype=torch.bfloat16))
 
 
 def _timing_case(rank, world):
