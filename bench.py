@@ -446,6 +446,7 @@ def run_gpu(args):
         line["roofline"] = None
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
+        line["cpu_baseline_all_cores"] = cpu_baseline_all_cores(seconds=args.cpu_seconds)
     if args.extra:
         line["extra_kernels"] = extra_kernels(dev, peaks)
     print(json.dumps(line))
@@ -495,6 +496,101 @@ def cpu_baseline(seconds: float = 10.0) -> dict:
             "sample": f"{steps} full step(s) of the workload (8 x 4096x4096 cast+transpose+amax "
                       f"+ update) through the single-threaded C oracle, {dt:.1f} s, on "
                       f"{os.cpu_count()} host cores (1 used)"}
+
+
+def _oracle_rows_worker(shm_name, n_inputs, conn):
+    """Spawned worker of cpu_baseline_all_cores: attaches the shared inputs,
+    then casts the row blocks it is sent with the oracle as it stands and
+    answers each with the block's amax."""
+    from multiprocessing import shared_memory
+
+    import numpy as np
+
+    import oracle
+    shm = shared_memory.SharedMemory(name=shm_name)
+    try:
+        xs = np.ndarray((n_inputs, ROWS, COLS), dtype=np.uint16, buffer=shm.buf)
+        conn.send("ready")
+        while True:
+            msg = conn.recv()
+            if msg is None:
+                break
+            k, r0, r1, scale = msg
+            r = oracle.cast_transpose(xs[k, r0:r1], scale, oracle.E4M3)
+            conn.send(float(r["amax"]))
+        del xs
+    finally:
+        shm.close()
+
+
+def cpu_baseline_all_cores(seconds: float = 10.0) -> dict:
+    """The oracle on every host core: each cast of the step is split into
+    row blocks, one per spawned worker process (the oracle's code as it
+    stands, run on a block of rows); the amaxes are merged and the update run
+    in this process before the next cast, which needs its scale."""
+    import multiprocessing as mp
+    from multiprocessing import shared_memory
+
+    import numpy as np
+
+    import oracle
+    xs = _oracle_inputs()
+    n = len(xs)
+    workers = max(1, os.cpu_count() or 1)
+    shm = shared_memory.SharedMemory(create=True, size=n * ROWS * COLS * 2)
+    procs, conns = [], []
+    try:
+        shared = np.ndarray((n, ROWS, COLS), dtype=np.uint16, buffer=shm.buf)
+        shared[:] = np.stack(xs)
+        ctx = mp.get_context("spawn")
+        for _ in range(workers):
+            a, b = ctx.Pipe()
+            p = ctx.Process(target=_oracle_rows_worker, args=(shm.name, n, b), daemon=True)
+            p.start()
+            procs.append(p)
+            conns.append(a)
+        for c in conns:
+            if not c.poll(300) or c.recv() != "ready":
+                raise RuntimeError("oracle worker did not start")
+        bounds = [ROWS * w // workers for w in range(workers + 1)]
+        hist = np.zeros((HIST_LEN, 1), np.float32)
+        scale, sinv = np.ones(1, np.float32), np.ones(1, np.float32)
+
+        def step():
+            nonlocal hist, scale, sinv
+            for k in range(n):
+                for w, c in enumerate(conns):
+                    c.send((k, bounds[w], bounds[w + 1], float(scale[0])))
+                a = np.float32(hist[0, 0])
+                for c in conns:
+                    a = np.float32(max(a, np.float32(c.recv())))   # amaxes are >= 0 (no NaN here)
+                hist[0, 0] = a
+                hist, scale, sinv = oracle.amax_and_scale_update(hist, scale, sinv, oracle.E4M3, 0)
+
+        step()                                   # warm-up
+        steps, t0 = 0, time.perf_counter()
+        while True:
+            step()
+            steps += 1
+            if time.perf_counter() - t0 >= seconds:
+                break
+        dt = time.perf_counter() - t0
+        del shared
+    finally:
+        for c in conns:
+            try:
+                c.send(None)
+            except Exception:
+                pass
+        for p in procs:
+            p.join(timeout=30)
+        shm.close()
+        shm.unlink()
+    return {"value": round(steps * STEP_BYTES / dt / 1e9, 4), "unit": UNIT, "cores": workers,
+            "kind": "oracle",
+            "sample": f"{steps} full step(s) of the workload; each of the 8 casts split into "
+                      f"{workers} row blocks run by {workers} spawned processes of the C oracle "
+                      f"(as it stands), the update in between; {dt:.1f} s"}
 
 
 def run_reference(args):
