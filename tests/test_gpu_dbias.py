@@ -165,3 +165,31 @@ def test_db_of_inf_and_nan_columns(shape, db_dtype):
         bits = db.view(torch.int16).cpu().numpy().view(np.uint16)
         assert bits[7] == 0x7FFF and bits[9] == 0x7FFF      # canonical NaN (the oracle's reading)
         assert np.array_equal(bits[[3, 5]], oracle.dbias_bf16(x_cpu)[[3, 5]])
+
+
+def test_gradient_8192x12288_bf16_db_two_steps():
+    """The gradient workload with a bf16 db, in the same two steps as the fp32
+    case: scale 1, then the scale the update derives from the first amax."""
+    dy = workloads.gradient_matrix("cuda")
+    x_cpu = dy.cpu()
+    rows, cols = dy.shape
+    q, qt = ct.empty_outputs(dy)
+    ws = torch.empty(ct.dbias_workspace_size(rows, cols), dtype=torch.uint8, device="cuda")
+    hist = np.zeros((16, 1), np.float32)
+    s_val = 1.0
+    for step in range(2):
+        db = torch.empty(cols, dtype=torch.bfloat16, device="cuda")
+        a, si = scalar(0.0), scalar(0.0)
+        ct.fp8_dbias_cast_transpose(dy, scalar(s_val), a, si, q, qt, db, ws, ct.E5M2)
+        torch.cuda.synchronize()
+        ref = oracle.cast_transpose(x_cpu, s_val, ct.E5M2)
+        assert np.array_equal(q.cpu().numpy(), ref["q"]), step
+        assert np.array_equal(qt.cpu().numpy(), ref["qt"]), step
+        assert f32_bits(a.item()) == f32_bits(ref["amax"]), step
+        bits = db.view(torch.int16).cpu().numpy().view(np.uint16)
+        assert dbias_bf16_tolerance_ok(bits, x_cpu), step
+        assert np.mean(bits == oracle.dbias_bf16(x_cpu)) >= 0.99, step
+        hist[0, 0] = ref["amax"]
+        hist, s_arr, _ = oracle.amax_and_scale_update(hist, np.float32([s_val]), np.ones(1, np.float32),
+                                                      ct.E5M2, 0)
+        s_val = float(s_arr[0])

@@ -66,7 +66,8 @@ def _run_with_workspace(dy, scale, fmt):
             "db": db.cpu().numpy(), "amax": a.item(), "scale_inv": si.item()}
 
 
-@pytest.mark.parametrize("shape,fmt", [((2048, 4096), ct.E5M2), ((1000, 1030), ct.E4M3)])
+@pytest.mark.parametrize("shape,fmt", [((2048, 4096), ct.E5M2), ((1000, 1030), ct.E4M3),
+                                       ((8192, 16384), ct.E5M2)])   # the largest it accepts
 def test_noalloc_matches_workspace_version_twice(shape, fmt):
     ct.device_error(clear=True)
     rows, cols = shape
