@@ -78,8 +78,11 @@ bool shape_ok(int64_t rows, int64_t cols) {
     return rows <= (int64_t(1) << 40) / cols;
 }
 
+// The fast kernels store 16-row blocks of the transpose as 16-byte vectors
+// (rows % 16) and read 8-element row chunks as 16-byte vectors (cols % 8,
+// which also makes the TMA row stride a multiple of 16 bytes).
 bool fast_shape(int64_t rows, int64_t cols) {
-    return rows % 16 == 0 && cols % 16 == 0 && rows <= kMaxDim && cols <= kMaxDim;
+    return rows % 16 == 0 && cols % 8 == 0 && rows <= kMaxDim && cols <= kMaxDim;
 }
 
 // Checks shared by the single-tensor cast entry points.

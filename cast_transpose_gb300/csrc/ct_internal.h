@@ -95,7 +95,7 @@ cudaError_t launch_fast_list(const FastParams<kMaxListPerLaunch>& p, int fmt,
 
 // Direct-load path (ct_direct.cu): one CTA per 128x128 tile, x read with
 // plain 16-byte loads; same eligibility as the TMA path (rows % 16 == 0,
-// cols % 16 == 0, 16-byte aligned x, out and out_t).  Chosen for launches of
+// cols % 8 == 0, 16-byte aligned x, out and out_t).  Chosen for launches of
 // at least kDirectMinTiles tiles (at most INT32_MAX), where it sustains a
 // higher read+write rate than the persistent TMA kernel; the persistent
 // kernel keeps the smaller launches, whose tiles it spreads evenly and whose

@@ -49,7 +49,8 @@
  *     cols == 0 returns CT_OK without a launch and writes nothing (its
  *     pointers are then not checked and may be NULL).  A failed launch returns
  *     CT_ERR_CUDA.  Any shape and alignment is accepted.  Shapes with rows
- *     and cols multiples of 16 and 16-byte-aligned buffers take a fast path:
+ *     a multiple of 16 and cols a multiple of 8, with 16-byte-aligned
+ *     buffers, take a fast path:
  *     a persistent TMA-staged kernel for launches under 2048 tiles of
  *     128x128, a one-tile-per-CTA direct-load kernel from 2048 tiles on.
  *     Everything else takes a slower general kernel.  All give identical

@@ -224,3 +224,58 @@ def test_long_list_direct_then_persistent():
         assert np.array_equal(outs[i].cpu().numpy().reshape(r, c), ref["q"]), i
         assert np.array_equal(outs_t[i].cpu().numpy().reshape(c, r), ref["qt"]), i
         assert f32_bits(a[i]) == f32_bits(ref["amax"]), i
+
+
+@pytest.mark.parametrize("fmt", [ct.E4M3, ct.E5M2])
+@pytest.mark.parametrize("shape", [(4096, 8200), (2064, 16392), (256, 136), (1024, 1032), (16, 8),
+                                   (144, 24)])
+def test_cols_multiple_of_8(fmt, shape):
+    """cols % 16 == 8 takes the fast kernels (the direct kernel from 2048
+    tiles, the persistent one below): cast-transpose, cast only and dbias."""
+    rows, cols = shape
+    x_cpu = workloads.gradient_matrix("cpu", rows, cols, std=1e-2, outlier_fraction=1e-3)
+    got = cast_transpose_gpu(x_cpu.cuda(), 1.75, fmt, amax_in=0.0625)
+    ref = oracle.cast_transpose(x_cpu, 1.75, fmt, amax_in=0.0625)
+    assert_same_cast(got, ref)
+    n = rows * cols
+    q = Guarded(n)
+    s, a, si = scalar(1.75), scalar(0.0), scalar(0.0)
+    ct.fp8_cast(x_cpu.cuda(), s, a, si, q.t, fmt)
+    torch.cuda.synchronize()
+    q.check()
+    assert np.array_equal(q.numpy().reshape(rows, cols), ref["q"])
+    q2, qt2 = Guarded(n), Guarded(n)
+    db = Guarded(cols, dtype=torch.float32)
+    ws = torch.empty(ct.dbias_workspace_size(rows, cols), dtype=torch.uint8, device="cuda")
+    ct.fp8_dbias_cast_transpose(x_cpu.cuda(), scalar(1.75), scalar(0.0), scalar(0.0), q2.t, qt2.t,
+                                db.t, ws, fmt)
+    torch.cuda.synchronize()
+    for g in (q2, qt2, db):
+        g.check()
+    assert np.array_equal(q2.numpy().reshape(rows, cols), ref["q"])
+    assert np.array_equal(qt2.numpy().reshape(cols, rows), ref["qt"])
+    assert dbias_tolerance_ok(db.numpy(), oracle.dbias(x_cpu), x_cpu)
+
+
+def test_list_with_cols_multiple_of_8():
+    shapes = [(1024, 1032), (4096, 4104), (16, 8), (528, 200)]
+    xs_cpu = [workloads.normal_bf16(r, c, 7.0, 8100 + i) for i, (r, c) in enumerate(shapes)]
+    n = len(xs_cpu)
+    scales = torch.tensor([1.0, 2.0, 0.5, 4.0], device="cuda")
+    amax = torch.zeros(n, device="cuda")
+    sinv = torch.zeros(n, device="cuda")
+    outs = [Guarded(x.numel()) for x in xs_cpu]
+    outs_t = [Guarded(x.numel()) for x in xs_cpu]
+    ct.fp8_multi_cast_transpose([x.cuda() for x in xs_cpu], [scales[i:i + 1] for i in range(n)],
+                                [amax[i:i + 1] for i in range(n)], [sinv[i:i + 1] for i in range(n)],
+                                [o.t for o in outs], [o.t for o in outs_t], ct.E4M3)
+    torch.cuda.synchronize()
+    a = amax.cpu().numpy()
+    for i, x in enumerate(xs_cpu):
+        r, c = x.shape
+        outs[i].check()
+        outs_t[i].check()
+        ref = oracle.cast_transpose(x, float(scales[i].item()), ct.E4M3)
+        assert np.array_equal(outs[i].numpy().reshape(r, c), ref["q"]), i
+        assert np.array_equal(outs_t[i].numpy().reshape(c, r), ref["qt"]), i
+        assert f32_bits(a[i]) == f32_bits(ref["amax"]), i
