@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libct_gb300.so")
 SOURCES = ["ct_api.cu", "ct_fast.cu", "ct_direct.cu", "ct_general.cu", "ct_noalloc.cu"]
-HEADERS = ["ct_internal.h", "ct_device.cuh", "ct_update.cuh"]
+HEADERS = ["ct_internal.h", "ct_device.cuh", "ct_update.cuh", "ct_gen_io.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr"]
 

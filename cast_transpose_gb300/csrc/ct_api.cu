@@ -115,6 +115,14 @@ bool fast_eligible(const void* x, int64_t rows, int64_t cols, const void* out, c
            (out_t == nullptr || aligned(out_t, 16)) && encode_fn() != nullptr;
 }
 
+// rows % 16 != 0 with whole 16-byte row chunks: the direct-load kernel, whose
+// transposed stores then take any alignment (the last 16-row block short).
+bool ragged_rows_eligible(const void* x, int64_t rows, int64_t cols, const void* out,
+                          const void* out_t) {
+    return rows % 16 != 0 && cols % 8 == 0 && rows <= kMaxDim && cols <= kMaxDim &&
+           aligned(x, 16) && aligned(out, 16) && (out_t == nullptr || aligned(out_t, 16));
+}
+
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? CT_OK : CT_ERR_CUDA; }
 
 void fill_tensor(FastTensor& t, const void* out, const void* out_t, const float* scale,
@@ -140,9 +148,10 @@ int cast_impl(const void* x, int64_t rows, int64_t cols, const float* scale, flo
               const float* noop, cudaStream_t stream, int64_t* runs_out = nullptr,
               bool x_ready = false) {
     const int64_t R = (rows + ct::kTileRows - 1) / ct::kTileRows;
-    if (fast_eligible(x, rows, cols, out, out_t)) {
+    const bool ragged_rows = ragged_rows_eligible(x, rows, cols, out, out_t);
+    if (ragged_rows || fast_eligible(x, rows, cols, out, out_t)) {
         const int64_t tiles = R * ((cols + ct::kTileCols - 1) / ct::kTileCols);
-        if (tiles >= ct::kDirectMinTiles && tiles <= INT32_MAX) {
+        if ((ragged_rows || tiles >= ct::kDirectMinTiles) && tiles <= INT32_MAX) {
             DirectParams<1> d;
             std::memset(&d, 0, sizeof(d));
             d.x[0] = static_cast<const uint16_t*>(x);
@@ -154,6 +163,8 @@ int cast_impl(const void* x, int64_t rows, int64_t cols, const float* scale, flo
             if (runs_out) *runs_out = R;
             return cuda_status(ct::launch_direct(d, fmt, partial != nullptr, out_t ? 0 : 1, stream));
         }
+    }
+    if (fast_eligible(x, rows, cols, out, out_t)) {
         FastParams<1> p;
         std::memset(&p, 0, sizeof(p));
         if (!encode_bf16_map(&p.map[0], x, rows, cols)) return CT_ERR_CUDA;
@@ -314,7 +325,9 @@ int multi_impl(const ct_tensor_desc* descs, const int* fmts, int n, int fmt,
                     if (overlap(r1, r2)) return CT_ERR_ALIAS;
         }
     }
-    // fast entries go into list launches of up to kMaxListPerLaunch tensors
+    // fast entries go into list launches of up to kMaxListPerLaunch tensors;
+    // the others go through the single-tensor dispatch (the direct kernel for
+    // rows % 16 != 0 with whole row chunks, else the general kernel)
     std::vector<int> fast, general;
     for (int i = 0; i < n; ++i) {
         const ct_tensor_desc& d = descs[i];

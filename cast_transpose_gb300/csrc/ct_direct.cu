@@ -24,6 +24,7 @@
 // count (thousands of CTAs, many waves of 152 SMs x 4); the TMA kernel keeps
 // the launches too small for that to pay.
 #include "ct_device.cuh"
+#include "ct_gen_io.cuh"
 #include "ct_internal.h"
 
 #include <climits>
@@ -161,14 +162,25 @@ __global__ void __launch_bounds__(kDirectThreads, kDirectMinBlocks)
         for (int g = 0; g < 4; ++g)
             dev::transpose4x4(rw[4 * g], rw[4 * g + 1], rw[4 * g + 2], rw[4 * g + 3], o[0][g],
                               o[1][g], o[2][g], o[3][g]);
-        const int64_t row = row0 + 16 * b;   // rows % 16 == 0: the block is whole
-        if (row < rows) {
+        const int64_t row = row0 + 16 * b;
+        if ((rows & 15) == 0) {   // whole, 16-byte aligned blocks
+            if (row < rows) {
 #pragma unroll
-            for (int kq = 0; kq < 4; ++kq) {
-                const int64_t col = col0 + 4 * w + kq;
-                if (col < cols)
-                    __stcs(reinterpret_cast<uint4*>(T.out_t + col * rows + row),
-                           make_uint4(o[kq][0], o[kq][1], o[kq][2], o[kq][3]));
+                for (int kq = 0; kq < 4; ++kq) {
+                    const int64_t col = col0 + 4 * w + kq;
+                    if (col < cols)
+                        __stcs(reinterpret_cast<uint4*>(T.out_t + col * rows + row),
+                               make_uint4(o[kq][0], o[kq][1], o[kq][2], o[kq][3]));
+                }
+            }
+        } else {                  // rows % 16 != 0: any alignment, the last block short
+            const int nr = row >= rows ? 0 : (rows - row >= 16 ? 16 : static_cast<int>(rows - row));
+            if (nr > 0) {
+#pragma unroll
+                for (int kq = 0; kq < 4; ++kq) {
+                    const int64_t col = col0 + 4 * w + kq;
+                    if (col < cols) gen::store16(T.out_t + col * rows + row, o[kq], nr);
+                }
             }
         }
     }

@@ -279,3 +279,37 @@ def test_list_with_cols_multiple_of_8():
         assert np.array_equal(outs[i].numpy().reshape(r, c), ref["q"]), i
         assert np.array_equal(outs_t[i].numpy().reshape(c, r), ref["qt"]), i
         assert f32_bits(a[i]) == f32_bits(ref["amax"]), i
+
+
+@pytest.mark.parametrize("fmt", [ct.E4M3, ct.E5M2])
+@pytest.mark.parametrize("shape", [(4100, 8192), (1000, 1024), (17, 8), (130, 4096), (4097, 136),
+                                   (2063, 8200), (1, 512)])
+def test_rows_not_multiple_of_16(fmt, shape):
+    """rows % 16 != 0, cols % 8 == 0, aligned buffers: the direct kernel with
+    transposed blocks at any alignment (the last one short), at every size;
+    cast-transpose, cast only and dbias."""
+    rows, cols = shape
+    x_cpu = workloads.gradient_matrix("cpu", rows, cols, std=1e-2, outlier_fraction=1e-3)
+    got = cast_transpose_gpu(x_cpu.cuda(), 3.25, fmt)
+    ref = oracle.cast_transpose(x_cpu, 3.25, fmt)
+    assert_same_cast(got, ref)
+    n = rows * cols
+    q2, qt2 = Guarded(n), Guarded(n)
+    db = Guarded(cols, dtype=torch.float32)
+    ws = torch.empty(ct.dbias_workspace_size(rows, cols), dtype=torch.uint8, device="cuda")
+    ws.fill_(0x7F)
+    ct.fp8_dbias_cast_transpose(x_cpu.cuda(), scalar(3.25), scalar(0.0), scalar(0.0), q2.t, qt2.t,
+                                db.t, ws, fmt)
+    torch.cuda.synchronize()
+    for g in (q2, qt2, db):
+        g.check()
+    assert np.array_equal(q2.numpy().reshape(rows, cols), ref["q"])
+    assert np.array_equal(qt2.numpy().reshape(cols, rows), ref["qt"])
+    assert dbias_tolerance_ok(db.numpy(), oracle.dbias(x_cpu), x_cpu)
+    q = Guarded(n)
+    s, a, si = scalar(3.25), scalar(0.0), scalar(0.0)
+    ct.fp8_cast(x_cpu.cuda(), s, a, si, q.t, fmt)
+    torch.cuda.synchronize()
+    q.check()
+    assert np.array_equal(q.numpy().reshape(rows, cols), ref["q"])
+    assert f32_bits(a.item()) == f32_bits(ref["amax"])
