@@ -120,3 +120,36 @@ def test_fp8_transpose_general(shape, in_shift):
     torch.cuda.synchronize()
     out.check()
     assert np.array_equal(out.numpy().reshape(cols, rows), oracle.fp8_transpose(q_cpu.numpy()))
+
+
+def test_random_shapes_offsets_and_paths():
+    """A seeded sweep of 200 cases: rows and cols in [1, 700] (multiples of 8 and
+    16 drawn often, so every kernel is reached), x shifted by 0..7 elements,
+    q and qT by 0..15 bytes, both formats, a random scale: the full outputs
+    of the cast-transpose and the dbias variant against the oracle."""
+    rng = np.random.default_rng(20261202)
+    for case in range(200):
+        pick = rng.integers(0, 3, size=2)
+        rows = int([rng.integers(1, 701), 16 * rng.integers(1, 44), 8 * rng.integers(1, 88)][pick[0]])
+        cols = int([rng.integers(1, 701), 16 * rng.integers(1, 44), 8 * rng.integers(1, 88)][pick[1]])
+        x_shift = int(rng.integers(0, 8)) if rng.random() < 0.5 else 0
+        out_shift = int(rng.integers(0, 16)) if rng.random() < 0.5 else 0
+        fmt = int(rng.integers(0, 2))
+        scale = float(np.float32(2.0 ** rng.uniform(-6, 6)))
+        x_cpu = workloads.normal_bf16(rows, cols, float(rng.uniform(0.1, 100)), 9000 + case)
+        x = _shifted(x_cpu, x_shift)
+        got = cast_transpose_gpu(x, scale, fmt, out_offset=out_shift)
+        ref = oracle.cast_transpose(x_cpu, scale, fmt)
+        assert_same_cast(got, ref)
+        n = rows * cols
+        q, qt = Guarded(n, offset=out_shift), Guarded(n, offset=out_shift)
+        db = Guarded(cols, dtype=torch.float32)
+        ws = torch.empty(ct.dbias_workspace_size(rows, cols), dtype=torch.uint8, device="cuda")
+        ct.fp8_dbias_cast_transpose(x, scalar(scale), scalar(0.0), scalar(0.0), q.t, qt.t, db.t, ws,
+                                    fmt)
+        torch.cuda.synchronize()
+        for g in (q, qt, db):
+            g.check()
+        assert np.array_equal(q.numpy().reshape(rows, cols), ref["q"]), (case, rows, cols)
+        assert np.array_equal(qt.numpy().reshape(cols, rows), ref["qt"]), (case, rows, cols)
+        assert dbias_tolerance_ok(db.numpy(), oracle.dbias(x_cpu), x_cpu), (case, rows, cols)
