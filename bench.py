@@ -378,7 +378,8 @@ def run_gpu(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16->fp8 (fp32 scale arithmetic)",
+        "dtype": "f32",
+        "dtype_note": "bf16 in, FP8 (E4M3) codes out; the scale product is one fp32 multiply",
         "data": "synthetic (seeded N(0,0.02) bf16, resident in HBM)",
         "config": {
             "workload": WORKLOAD,
@@ -625,7 +626,8 @@ def run_reference(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16->fp8 (fp32 scale arithmetic)",
+        "dtype": "f32",
+        "dtype_note": "bf16 in, FP8 (E4M3) codes out; the scale product is one fp32 multiply",
         "data": "synthetic (seeded N(0,0.02) bf16)",
         "config": {"workload": WORKLOAD, "shape": [ROWS, COLS], "fp8": "E4M3",
                    "amax_history_len": HIST_LEN, "margin": 0, "parallelism": "host, 1 thread"},
