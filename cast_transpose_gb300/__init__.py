@@ -90,6 +90,8 @@ def lib() -> ctypes.CDLL:
             L.ct_device_error.argtypes = [c.POINTER(c.c_uint), i32]
             L.ct_selftest_bounded_wait.argtypes = [c.c_uint, vp]
             L.ct_selftest_bounded_wait.restype = i32
+            L.ct_fp8_convert_f32.argtypes = [vp, i64, i32, vp, vp]
+            L.ct_fp8_convert_f32.restype = i32
             for name in ("fp8_cast_transpose", "fp8_cast_transpose_ex", "fp8_cast",
                          "fp8_dbias_cast_transpose", "fp8_dbias_cast_transpose_ex",
                          "fp8_multi_cast_transpose", "fp8_multi_cast_transpose_ex",
@@ -257,6 +259,14 @@ def fp8_transpose(q, out_t, noop_flag=None, stream=None) -> None:
     rows, cols = _rc(q)
     _check(lib().fp8_transpose(_dev(q, "q", _U8), rows, cols, _dev(out_t, "out_t", _U8, rows * cols),
                                _opt(noop_flag, "noop_flag"), _stream(stream)))
+
+
+def fp8_convert_f32(x, out, fmt=E4M3, stream=None) -> None:
+    """out[i] = FP8 code of the fp32 value x[i] (the cast kernels' conversion
+    step without the scale); x fp32, out uint8, both contiguous, same size."""
+    n = x.numel()
+    _check(lib().ct_fp8_convert_f32(_dev(x, "x", torch.float32), n, fmt, _dev(out, "out", _U8, n),
+                                    _stream(stream)))
 
 
 def device_error(clear: bool = False) -> int:

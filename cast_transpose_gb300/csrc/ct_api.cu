@@ -443,6 +443,17 @@ int fp8_transpose(const void* in, int64_t rows, int64_t cols, void* out, const f
                                             static_cast<cudaStream_t>(stream)));
 }
 
+int ct_fp8_convert_f32(const float* in, int64_t n, int fmt, void* out, void* stream) {
+    if (fmt != CT_E4M3 && fmt != CT_E5M2) return CT_ERR_FORMAT;
+    if (n < 0 || n > (int64_t(1) << 40)) return CT_ERR_SHAPE;
+    if (n == 0) return CT_OK;
+    if (!in || !out) return CT_ERR_NULL;
+    if (!aligned(in, 4)) return CT_ERR_ALIGN;
+    if (overlap(range_of(in, 4 * n), range_of(out, n))) return CT_ERR_ALIAS;
+    return cuda_status(ct::launch_convert_f32(in, n, fmt, static_cast<uint8_t*>(out),
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 int ct_selftest_bounded_wait(unsigned int limit_us, void* stream) {
     if (limit_us == 0 || limit_us > 1000000u) return CT_ERR_ARG;
     return cuda_status(ct::launch_wait_selftest(limit_us, static_cast<cudaStream_t>(stream)));

@@ -453,6 +453,27 @@ __global__ void __launch_bounds__(256) transpose_general_kernel(const uint8_t* _
     }
 }
 
+// ---------------------------------------------------------------------------
+// The conversion step alone: out[i] = fp8(in[i]) through dev::cvt_fp8x2, the
+// routine every cast kernel applies to x * scale.  Grid-stride over pairs of
+// values; a trailing odd value is converted with a zero partner whose code is
+// not stored.
+template <int FMT>
+__global__ void __launch_bounds__(256) convert_f32_kernel(const float* __restrict__ in, int64_t n,
+                                                          uint8_t* __restrict__ out) {
+    dev::pdl_launch_dependents();
+    dev::pdl_wait();
+    const int64_t pairs = (n + 1) / 2;
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t k = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; k < pairs; k += stride) {
+        const int64_t i = 2 * k;
+        const bool two = i + 1 < n;
+        const uint32_t c = dev::cvt_fp8x2<FMT>(in[i], two ? in[i + 1] : 0.0f);
+        out[i] = static_cast<uint8_t>(c);
+        if (two) out[i + 1] = static_cast<uint8_t>(c >> 8);
+    }
+}
+
 unsigned grid_for(int64_t tiles, int64_t cap) {
     if (tiles < 1) tiles = 1;
     return static_cast<unsigned>(tiles < cap ? tiles : cap);
@@ -495,6 +516,13 @@ cudaError_t launch_scale_update(float* hist, float* scale, float* scale_inv, int
     const dim3 grid(static_cast<unsigned>((count + 127) / 128)), block(128);
     return launch_pdl(scale_update_long_kernel, grid, block, 0, stream, hist, scale, scale_inv,
                       hist_len, count, stride, fp8_max, two_pow_margin, most_recent, noop);
+}
+
+cudaError_t launch_convert_f32(const float* in, int64_t n, int fmt, uint8_t* out,
+                               cudaStream_t stream) {
+    const dim3 grid(grid_for(((n + 1) / 2 + 255) / 256, 152 * 16)), block(256);
+    return fmt == 0 ? launch_pdl(convert_f32_kernel<0>, grid, block, 0, stream, in, n, out)
+                    : launch_pdl(convert_f32_kernel<1>, grid, block, 0, stream, in, n, out);
 }
 
 cudaError_t launch_transpose(const uint8_t* in, int64_t rows, int64_t cols, uint8_t* out,

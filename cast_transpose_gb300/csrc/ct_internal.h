@@ -166,6 +166,10 @@ cudaError_t launch_scale_update(float* hist, float* scale, float* scale_inv, int
 cudaError_t launch_transpose(const uint8_t* in, int64_t rows, int64_t cols, uint8_t* out,
                              const float* noop, bool fast, cudaStream_t stream);
 
+// FP8 conversion of n fp32 values (no scale): the cast kernels' conversion step.
+cudaError_t launch_convert_f32(const float* in, int64_t n, int fmt, uint8_t* out,
+                               cudaStream_t stream);
+
 // Diagnostic word (device of the calling thread).
 cudaError_t read_device_error(unsigned* value, bool clear);
 

@@ -16,7 +16,8 @@ Workloads (all row-major bf16):
     seeded random positions set to +-5.0 with seeded signs     (seed 1003)
   * a list of 48 tensors cycling through 6144x12288, 12288x6144, 18432x6144
     and 6144x24576, N(0, 0.02); tensors 7 and 30 all zero, tensors 15 and 44
-    rescaled in fp32 so that max|x| = 1e-30 before rounding  (seed 1004 + i)
+    rescaled in fp32 so that max|x| = 1e-30 before rounding
+    (seed 1004000 + i; shard s of a layer, e.g. on rank s: + 100000 * s)
   * activation 16384x12288, 0.5 * Student-t with 3 degrees of freedom built
     as z0 / sqrt((z1^2 + z2^2 + z3^2) / 3) from four seeded normals (seed 1005)
 """
@@ -80,11 +81,13 @@ def multi_shape(i: int, shapes=MULTI_SHAPES) -> tuple:
 
 
 def multi_tensor(i: int, device="cpu", shapes=MULTI_SHAPES,
-                 zero=MULTI_ZERO, tiny=MULTI_TINY) -> torch.Tensor:
+                 zero=MULTI_ZERO, tiny=MULTI_TINY, shard: int = 0) -> torch.Tensor:
+    """Tensor i of the list; `shard` > 0 draws another shard of the same
+    layer (another seed, same shape and recipe), e.g. one per rank."""
     rows, cols = multi_shape(i, shapes)
     if i in zero:
         return torch.zeros(rows, cols, dtype=torch.bfloat16, device=device)
-    g = _gen(SEED_MULTI * 1000 + i, device)
+    g = _gen(SEED_MULTI * 1000 + i + 100000 * shard, device)
     x = torch.randn(rows, cols, generator=g, device=device, dtype=torch.float32) * 0.02
     if i in tiny:
         x = x * (1e-30 / x.abs().max())
@@ -92,8 +95,8 @@ def multi_tensor(i: int, device="cpu", shapes=MULTI_SHAPES,
 
 
 def multi_list(device="cpu", count: int = MULTI_COUNT, shapes=MULTI_SHAPES,
-               zero=MULTI_ZERO, tiny=MULTI_TINY) -> list:
-    return [multi_tensor(i, device, shapes, zero, tiny) for i in range(count)]
+               zero=MULTI_ZERO, tiny=MULTI_TINY, shard: int = 0) -> list:
+    return [multi_tensor(i, device, shapes, zero, tiny, shard) for i in range(count)]
 
 
 def activation_matrix(device="cpu", rows: int = 16384, cols: int = 12288,

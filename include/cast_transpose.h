@@ -337,6 +337,26 @@ int fp8_dbias_cast_transpose_noalloc(const void* dy, int64_t rows, int64_t cols,
                                      const float* noop_flag, void* stream);
 
 /*
+ * ct_fp8_convert_f32 -- the FP8 conversion step of the cast kernels applied
+ * to fp32 values as given: out[i] = fp8(in[i]), round to nearest even, values
+ * beyond the largest normal and +-Inf saturate to +-max, NaN gives 0x7F, no
+ * flush-to-zero.  It is the same device routine every cast kernel applies to
+ * the product x * scale ("[PyTorch] cuda graph support": cast_transpose(dy);
+ * FP8 formats as in the OCP OFP8 specification), exposed without the scale,
+ * amax and layout around it so that the conversion itself can be checked
+ * against a reference over any set of fp32 values (every bit pattern, say).
+ *
+ *   in    fp32 [n], 4-byte aligned (read only)
+ *   n     number of values (>= 0; 0 returns CT_OK and launches nothing)
+ *   fmt   CT_E4M3 or CT_E5M2
+ *   out   uint8 [n] output, any alignment; must not overlap `in`
+ *
+ * One launch on `stream`.  Errors: CT_ERR_NULL, CT_ERR_SHAPE (n < 0),
+ * CT_ERR_ALIGN, CT_ERR_FORMAT, CT_ERR_ALIAS, CT_ERR_CUDA.
+ */
+int ct_fp8_convert_f32(const float* in, int64_t n, int fmt, void* out, void* stream);
+
+/*
  * ct_device_error -- diagnostic word of the current device.  Kernels that
  * wait on an mbarrier give up after a bounded time (about two seconds)
  * instead of hanging, set a bit here and return early; in a correct run it

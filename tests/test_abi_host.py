@@ -193,3 +193,14 @@ def test_multi_ex_rejects(L):
     bad = (ctypes.c_int * 1)(7)
     assert L.fp8_multi_cast_transpose_ex(arr, bad, 1, None, None) == CT_ERR_FORMAT
     assert L.fp8_multi_cast_transpose_ex(None, None, 0, None, None) == CT_OK
+
+
+def test_fp8_convert_f32_rejects(L):
+    f = L.ct_fp8_convert_f32
+    assert f(X, 100, 2, Q, None) == CT_ERR_FORMAT
+    assert f(X, -1, 0, Q, None) == CT_ERR_SHAPE
+    assert f(None, 100, 0, Q, None) == CT_ERR_NULL
+    assert f(X, 100, 1, None, None) == CT_ERR_NULL
+    assert f(X + 2, 100, 0, Q, None) == CT_ERR_ALIGN
+    assert f(X, 100, 0, X + 399, None) == CT_ERR_ALIAS    # out starts inside the 400 input bytes
+    assert f(None, 0, 0, None, None) == CT_OK              # nothing to do, nothing launched

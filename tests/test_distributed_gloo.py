@@ -107,9 +107,8 @@ def test_dbias_allreduce_rejects_bf16():
 
 
 def _timing_case(rank, world):
-    t = torch.tensor([1.5 if rank == 0 else 2.25], dtype=torch.float64)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    import bench
+    return bench._max_over_ranks(1.5 if rank == 0 else 2.25, world)
 
 
 def test_max_over_ranks_gloo_world2():

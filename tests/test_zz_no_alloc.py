@@ -1,15 +1,16 @@
 """fp8_dbias_cast_transpose_noalloc: the dbias cast-transpose for callers
-that cannot allocate device memory (code running during CUDA-graph capture,
-inside an allocator or memory-pool callback, or under a runtime that has
-reserved all device memory up front).  Instead of a caller workspace it uses
-a fixed scratch array that the library keeps on the GPU.
+that cannot allocate device memory where they call it (code inside an
+allocator or memory-pool callback, where allocating again would recurse or
+deadlock, or a runtime that has reserved all device memory up front).
+Instead of a caller workspace it uses a fixed scratch array that the library
+keeps on the GPU.
 
-Checked through the C ABI against fp8_dbias_cast_transpose with a normal
-workspace, on two calls in a row with different inputs (the shared scratch
-keeps the previous call's contents, which must not leak into the next one):
-FP8 data, transpose, amax and scale_inv bit-exact, db within the dbias
-tolerance of the other tests.  This file sorts last so that a run stopping at
-its first failure has run everything else before it.
+Checked through the C ABI on two calls in a row with different inputs (the
+shared scratch keeps the previous call's contents, which must not leak into
+the next one), against both the oracle and fp8_dbias_cast_transpose with a
+normal workspace: FP8 data, transpose, amax and scale_inv bit-exact, db
+within the dbias tolerance of the other tests.  This file sorts last so that
+a run stopping at its first failure has run everything else before it.
 """
 import ctypes
 
@@ -18,8 +19,10 @@ import pytest
 import torch
 
 import cast_transpose_gb300 as ct
+import oracle
 from cast_transpose_gb300 import workloads
 from gpu_util import Guarded, dbias_tolerance_ok, f32_bits, scalar
+from oracle_pool import OraclePool
 
 pytestmark = pytest.mark.gpu
 
@@ -68,19 +71,37 @@ def _run_with_workspace(dy, scale, fmt):
 
 @pytest.mark.parametrize("shape,fmt", [((2048, 4096), ct.E5M2), ((1000, 1030), ct.E4M3),
                                        ((8192, 16384), ct.E5M2)])   # the largest it accepts
-def test_noalloc_matches_workspace_version_twice(shape, fmt):
+def test_noalloc_matches_oracle_and_workspace_version_twice(shape, fmt):
     ct.device_error(clear=True)
     rows, cols = shape
     inputs = [workloads.gradient_matrix("cuda", rows, cols, std=1e-3, outlier_fraction=1e-3),
               workloads.normal_bf16(rows, cols, 2.0, 4242, "cuda")]
-    for call, dy in enumerate(inputs):            # two calls in a row, different data
-        got = _run_noalloc(dy, 1.5, fmt)
-        ref = _run_with_workspace(dy, 1.5, fmt)
-        assert np.array_equal(got["q"], ref["q"]), f"call {call}: FP8 data differs"
-        assert np.array_equal(got["qt"], ref["qt"]), f"call {call}: transpose differs"
-        assert f32_bits(got["amax"]) == f32_bits(ref["amax"])
-        assert f32_bits(got["scale_inv"]) == f32_bits(ref["scale_inv"])
-        assert dbias_tolerance_ok(got["db"], ref["db"], dy.cpu()), f"call {call}: db differs"
+    with OraclePool() as pool:
+        for call, dy in enumerate(inputs):            # two calls in a row, different data
+            got = _run_noalloc(dy, 1.5, fmt)
+            dy_cpu = dy.cpu()
+            # the oracle: every byte of q and qT, amax, scale_inv, db
+            xin = pool.input_bf16(rows, cols)
+            xin[:] = dy_cpu.view(torch.int16).numpy().view(np.uint16)
+            q, qt = pool.output_q(rows, cols), pool.output_qt(rows, cols)
+            q[:] = got["q"].reshape(rows, cols)
+            qt[:] = got["qt"].reshape(cols, rows)
+            res = pool.check_cast_transpose(rows, cols, 1.5, fmt)
+            del xin, q, qt
+            assert res["bad_q"] == 0, (call, "FP8 data differs from the oracle", res["first_q"])
+            assert res["bad_qt"] == 0, (call, "transpose differs from the oracle", res["first_qt"])
+            assert f32_bits(got["amax"]) == f32_bits(res["amax"])
+            sinv_ref = oracle.cast_transpose(dy_cpu[:1], 1.5, fmt)["scale_inv"]
+            assert f32_bits(got["scale_inv"]) == f32_bits(sinv_ref)
+            assert dbias_tolerance_ok(got["db"], oracle.dbias(dy_cpu), dy_cpu), \
+                f"call {call}: db outside the tolerance of the oracle's column sums"
+            # the entry point with a caller workspace: the same bytes, db within tolerance
+            ref = _run_with_workspace(dy, 1.5, fmt)
+            assert np.array_equal(got["q"], ref["q"]), f"call {call}: FP8 data differs"
+            assert np.array_equal(got["qt"], ref["qt"]), f"call {call}: transpose differs"
+            assert f32_bits(got["amax"]) == f32_bits(ref["amax"])
+            assert f32_bits(got["scale_inv"]) == f32_bits(ref["scale_inv"])
+            assert dbias_tolerance_ok(got["db"], ref["db"], dy_cpu), f"call {call}: db differs"
     assert ct.device_error() == 0
 
 
