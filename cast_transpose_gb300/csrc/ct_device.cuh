@@ -142,6 +142,29 @@ __device__ __forceinline__ void consumer_sync(int count) {
     asm volatile("bar.sync 1, %0;" ::"r"(count) : "memory");
 }
 
+// Barrier among the 256 threads of thread group g of a CTA that runs several
+// independent groups (named barrier 1 + g).
+__device__ __forceinline__ void group_sync(int g) {
+    asm volatile("bar.sync %0, 256;" ::"r"(1 + g) : "memory");
+}
+
+// ---- compensated summation -----------------------------------------------------
+// Kahan sum in fp32 (error within a few fp32 ulps of the sum of magnitudes
+// for any number of terms, without fp64, which runs at a small fraction of
+// the fp32 rate on this GPU).  Once the running sum is not finite (an Inf or
+// NaN among the terms) the correction is dropped, so the sum keeps the plain
+// IEEE result (Inf, or NaN for Inf - Inf and NaN terms) instead of the
+// Inf - Inf of the correction term.
+struct Kahan {
+    float sum = 0.0f, comp = 0.0f;
+    __device__ __forceinline__ void add(float v) {
+        const float y = __fsub_rn(v, comp);
+        const float t = __fadd_rn(sum, y);
+        comp = isfinite(t) ? __fsub_rn(__fsub_rn(t, sum), y) : 0.0f;
+        sum = t;
+    }
+};
+
 // ---- TMA ---------------------------------------------------------------------
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t pol;
@@ -198,6 +221,33 @@ __device__ __forceinline__ void transpose4x4(uint32_t r0, uint32_t r1, uint32_t 
 // pass reads at once over all 32 banks, and keeps the two words of every
 // 8-byte row store adjacent (swz is even).
 __device__ __forceinline__ int swz(int r) { return 2 * ((r >> 3) & 15); }
+
+// Column-sum scratch of one tile: the 8 warps' sums of 128 columns.  Warp
+// w's 16 active lanes (chunk c) store columns 8c .. 8c+3 as one float4 at
+// w * kColsumStride + 4c and columns 8c+4 .. 8c+7 at w * kColsumStride + 80 +
+// 4c, so each store instruction covers 256 contiguous bytes (no bank
+// conflict) and the reads of 32 consecutive columns fall in 32 banks.
+constexpr int kColsumStride = 160;
+__device__ __forceinline__ int colsum_index(int w, int col) {
+    return w * kColsumStride + ((col & 7) >> 2) * 80 + 4 * (col >> 3) + (col & 3);
+}
+__device__ __forceinline__ void colsum_store(float* colsum, int warp, int c, const float (&cs)[8]) {
+    float* base = colsum + warp * kColsumStride + 4 * c;
+    *reinterpret_cast<float4*>(base) = make_float4(cs[0], cs[1], cs[2], cs[3]);
+    *reinterpret_cast<float4*>(base + 80) = make_float4(cs[4], cs[5], cs[6], cs[7]);
+}
+
+// ---- asynchronous copies into shared memory ----------------------------------
+// 16-byte copy from global (16-byte aligned) to shared memory, bypassing L1;
+// only the first src_bytes (1..16) are read, the rest of the 16 is zero.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
 
 // Max of the two bf16 magnitudes (sign cleared) of a packed pair, kept as a
 // pair: one AND and one native 16x2 unsigned max per word.

@@ -1,4 +1,4 @@
-// ct_direct.cu -- one-tile-per-CTA cast-transpose with direct vector loads (sm_103a).
+// ct_direct.cu -- one tile per 256 threads, cast-transpose with direct vector loads (sm_103a).
 //
 // Operation ("[PyTorch] cuda graph support", DbiasCastTranspose example;
 // "[PyTorch] Refactor FP8 workspaces in linear modules", Motivations): the
@@ -7,7 +7,7 @@
 // fp32 column sums of x -- for launches large enough to fill the GPU many
 // times over.
 //
-// Design: the CTA of 256 threads that owns tile (rt, ct) issues all of its
+// Design: the 256 threads that own tile (rt, ct) issue all of its
 // 128x128 bf16 tile as eight 16-byte loads per thread at once (16 threads
 // cover one 256-byte row segment, 128 KB in flight per SM at 4 resident
 // CTAs), then
@@ -15,29 +15,38 @@
 //     (16 threads write one 128-byte line) and into the XOR-swizzled FP8 copy
 //     of the tile in shared memory (dev::swz); keeps the amax as a SIMD max
 //     of bf16 magnitudes and, for dbias, 8 column sums per thread;
-//   * one __syncthreads;
+//   * one barrier among the tile's 256 threads;
 //   * pass 2: each thread gathers a 16-row x 4-column byte block of the copy,
 //     transposes it with byte permutes and writes four 16-byte vectors of qT
 //     (8 threads write one 128-byte line).
 // No pipeline state crosses tiles, so the kernel has no waits; the latency of
-// one tile's loads is hidden by the other resident CTAs.  Grids are the tile
-// count (thousands of CTAs, many waves of 152 SMs x 4); the TMA kernel keeps
-// the launches too small for that to pay.
+// one tile's loads is hidden by the other resident tiles.  Grids cover the
+// tile count (thousands of CTAs, many waves of 152 SMs x 4 tiles); the TMA
+// kernel keeps the launches too small for that to pay.
 #include "ct_device.cuh"
 #include "ct_gen_io.cuh"
 #include "ct_internal.h"
 
 #include <climits>
 
+
 namespace ct {
 namespace {
 
+// A tile is processed by 256 threads.  A CTA runs TPC tiles side by side:
+// 256 * TPC threads in TPC independent groups, group g on tile
+// blockIdx.x * TPC + g, each group with its own named barrier.  Registers
+// (64 per thread) allow 1024 threads per SM, i.e. 4 tiles in flight per SM
+// either way.  Cast + transpose runs 2 tiles per CTA: the same rate as 1
+// (6.87-6.89 against 6.89-6.91 TB/s on 16384x12288, back to back) while a
+// launch skipped by the noop flag starts half as many CTAs (6.8 against
+// 12.7 us); 4 tiles per CTA lost 10% (1 CTA per SM).  Cast only (6.84
+// against 6.96 TB/s) and dbias (75 against 64 us) keep 1 tile per CTA.
 constexpr int kDirectThreads = 256;
-#ifndef CT_DIRECT_MINB
-#define CT_DIRECT_MINB 4
-#endif
-constexpr int kDirectMinBlocks = CT_DIRECT_MINB;
 constexpr int kDirectWarps = kDirectThreads / 32;
+
+template <bool WRITE_T, bool DBIAS>
+constexpr int tiles_per_cta() { return WRITE_T && !DBIAS ? 2 : 1; }
 
 // The tensor of a list launch that owns global tile `tile`: the last entry
 // whose first tile is <= tile (entries are non-empty and in tile order).
@@ -56,8 +65,17 @@ __device__ __forceinline__ int owner(const DirectParams<NT>& p, int64_t tile) {
     }
 }
 
-template <int NT, int FMT, bool WRITE_T, bool DBIAS>
-__global__ void __launch_bounds__(kDirectThreads, kDirectMinBlocks)
+template <int TPC>
+__device__ __forceinline__ void tile_sync(int g) {
+    if constexpr (TPC == 1) __syncthreads();
+    else dev::group_sync(g);
+}
+
+using dev::colsum_index;
+using dev::kColsumStride;
+
+template <int NT, int FMT, bool WRITE_T, bool DBIAS, int TPC>
+__global__ void __launch_bounds__(kDirectThreads * TPC, 4 / TPC)
     direct_cast_transpose_kernel(const __grid_constant__ DirectParams<NT> p) {
     // The next kernel of the stream may be scheduled as soon as this grid's
     // last wave is resident; it waits for this grid on the device.
@@ -65,12 +83,17 @@ __global__ void __launch_bounds__(kDirectThreads, kDirectMinBlocks)
     dev::pdl_wait();
     if (p.noop != nullptr && *p.noop != 0.0f) return;
 
-    __shared__ __align__(16) uint8_t sq[WRITE_T ? kTileRows * kTileCols : 16];
-    __shared__ __align__(16) float colsum[DBIAS ? kDirectWarps * kTileCols : 4];
-    __shared__ unsigned s_amax[kDirectWarps];
+    __shared__ __align__(16) uint8_t sq_all[TPC][WRITE_T ? kTileRows * kTileCols : 16];
+    __shared__ __align__(16) float colsum_all[TPC][DBIAS ? kDirectWarps * kColsumStride : 4];
+    __shared__ unsigned s_amax_all[TPC][kDirectWarps];
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t tile = blockIdx.x;
+    const int g = TPC == 1 ? 0 : static_cast<int>(threadIdx.x / kDirectThreads);
+    const int tid = threadIdx.x % kDirectThreads, lane = tid & 31, warp = tid >> 5;
+    const int64_t tile = static_cast<int64_t>(blockIdx.x) * TPC + g;
+    if (tile >= p.total_tiles) return;   // a whole group of the last CTA: no barrier involves it
+    uint8_t* sq = sq_all[g];
+    float* colsum = colsum_all[g];
+    unsigned* s_amax = s_amax_all[g];
     const int ti = owner(p, tile);
     const FastTensor& T = p.t[ti];
     const int64_t rows = T.rows, cols = T.cols;
@@ -123,13 +146,9 @@ __global__ void __launch_bounds__(kDirectThreads, kDirectMinBlocks)
     if constexpr (DBIAS) {   // fold the warp's two row groups (lanes l, l + 16)
 #pragma unroll
         for (int j = 0; j < 8; ++j) cs[j] += __shfl_xor_sync(0xFFFFFFFFu, cs[j], 16);
-        if (lane < 16) {
-            float4* dst = reinterpret_cast<float4*>(colsum + warp * kTileCols + 8 * c);
-            dst[0] = make_float4(cs[0], cs[1], cs[2], cs[3]);
-            dst[1] = make_float4(cs[4], cs[5], cs[6], cs[7]);
-        }
+        if (lane < 16) dev::colsum_store(colsum, warp, c, cs);
     }
-    __syncthreads();
+    tile_sync<TPC>(g);
 
     if (tid == 0) {
         unsigned a = s_amax[0];
@@ -140,9 +159,9 @@ __global__ void __launch_bounds__(kDirectThreads, kDirectMinBlocks)
     }
     if constexpr (DBIAS) {   // one partial row per tile row, warps summed in order
         if (tid < kTileCols && col0 + tid < cols) {
-            float sum = colsum[tid];
+            float sum = colsum[colsum_index(0, tid)];
 #pragma unroll
-            for (int w = 1; w < kDirectWarps; ++w) sum += colsum[w * kTileCols + tid];
+            for (int w = 1; w < kDirectWarps; ++w) sum += colsum[colsum_index(w, tid)];
             p.partial[rt * cols + col0 + tid] = sum;
         }
     }
@@ -173,25 +192,34 @@ __global__ void __launch_bounds__(kDirectThreads, kDirectMinBlocks)
                                make_uint4(o[kq][0], o[kq][1], o[kq][2], o[kq][3]));
                 }
             }
-        } else {                  // rows % 16 != 0: any alignment, the last block short
-            const int nr = row >= rows ? 0 : (rows - row >= 16 ? 16 : static_cast<int>(rows - row));
-            if (nr > 0) {
+        } else {   // rows % 16 != 0: each column's segment of qT starts at any byte
+            const int L = static_cast<int>(rows - row0 < kTileRows ? rows - row0 : kTileRows);
 #pragma unroll
-                for (int kq = 0; kq < 4; ++kq) {
-                    const int64_t col = col0 + 4 * w + kq;
-                    if (col < cols) gen::store16(T.out_t + col * rows + row, o[kq], nr);
-                }
+            for (int kq = 0; kq < 4; ++kq) {
+                const int64_t col = col0 + 4 * w + kq;
+                gen::store_segment_x8(T.out_t + col * rows + row0, col < cols ? L : 0, o[kq], b);
             }
         }
     }
 }
 
+template <int NT, int FMT, bool WRITE_T, bool DBIAS, int TPC>
+cudaError_t launch_tpc(const DirectParams<NT>& p, cudaStream_t stream) {
+    const int64_t grid = (p.total_tiles + TPC - 1) / TPC;
+    return launch_pdl(direct_cast_transpose_kernel<NT, FMT, WRITE_T, DBIAS, TPC>,
+                      dim3(static_cast<unsigned>(grid)), dim3(kDirectThreads * TPC), 0, stream, p);
+}
+
 template <int NT, int FMT, bool WRITE_T, bool DBIAS>
 cudaError_t launch_one(const DirectParams<NT>& p, cudaStream_t stream) {
     if (p.total_tiles <= 0 || p.total_tiles > INT_MAX) return cudaErrorInvalidValue;
-    return launch_pdl(direct_cast_transpose_kernel<NT, FMT, WRITE_T, DBIAS>,
-                      dim3(static_cast<unsigned>(p.total_tiles)), dim3(kDirectThreads), 0, stream,
-                      p);
+    constexpr int TPC = tiles_per_cta<WRITE_T, DBIAS>();
+    // rows % 16 != 0 (single tensors only): 1 tile per CTA, measured faster
+    // for the transposed stores at any alignment (4.85 against 4.08 TB/s on
+    // 8191x12288)
+    if constexpr (NT == 1 && TPC != 1)
+        if (p.t[0].rows % 16 != 0) return launch_tpc<NT, FMT, WRITE_T, DBIAS, 1>(p, stream);
+    return launch_tpc<NT, FMT, WRITE_T, DBIAS, TPC>(p, stream);
 }
 
 }  // namespace

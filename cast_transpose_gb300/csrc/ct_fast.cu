@@ -49,12 +49,10 @@ namespace {
 constexpr int kStageBytes = kTileRows * kTileCols * 2;   // bf16 tile
 constexpr int kSqBytes = kTileRows * kTileCols;          // FP8 copy
 
-// Threads per CTA of the TMA kernels (256 or 512; compile-time constant).
-#ifndef CT_THREADS
-#define CT_THREADS 256
-#endif
-constexpr int kFastThreads = CT_THREADS;
-static_assert(kFastThreads == 256 || kFastThreads == 512, "256 or 512 threads");
+// Consumer threads per CTA of the TMA kernel (512 was measured on GB300 and
+// was slower; the mappings below are written for 256).
+constexpr int kFastThreads = 256;
+static_assert(kFastThreads == 256, "the pass-1 and pass-2 mappings assume 256 threads");
 constexpr int kWarps = kFastThreads / 32;
 constexpr int kColsumFloats = kWarps * kTileCols;         // [warp][col]
 
@@ -115,10 +113,7 @@ struct SmemLayout {
 // of every row it touches at the same time, not 128 scattered bytes.
 // Measured on GB300 (4096x4096 step): bands of 16 beat 8 by 1%, and 2, 4,
 // 32 and 64 were slower.
-#ifndef CT_BAND
-#define CT_BAND 16
-#endif
-constexpr uint32_t kBand = CT_BAND;
+constexpr uint32_t kBand = 16;
 
 __device__ __forceinline__ void tile_coords(uint32_t local, uint32_t tile_rows, uint32_t tile_cols,
                                             int32_t& rt, int32_t& ct) {
@@ -141,7 +136,7 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
     using L = SmemLayout<STAGES, WRITE_T, DBIAS>;
     // Rows of the staged tile loaded per batch in pass 1: all at once for the
     // most loads in flight, 4 when registers are tight.
-    constexpr int kBatch = (DBIAS && (MINB > 1 || kFastThreads == 512)) ? 4 : 8 * 256 / kFastThreads;
+    constexpr int kBatch = (DBIAS && MINB > 1) ? 4 : 8;
     // When the next kernel of the stream may be scheduled.  Without dbias it
     // is typically a one-warp scale update or the next cast, which either
     // fits beside this kernel or cannot start before its CTAs leave: let it be
@@ -297,13 +292,13 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
     for (int j = 0; j < 8; ++j) cs[j] = 0.0f;
 
     // pass-1 mapping: column chunk c (8 columns), rows rg + kRowStep*it
-    constexpr int kRowStep = kFastThreads / 16;           // 16 or 32
-    constexpr int kRowsPerThread = kTileRows / kRowStep;  // 8 or 4
+    constexpr int kRowStep = kFastThreads / 16;           // 16
+    constexpr int kRowsPerThread = kTileRows / kRowStep;  // 8
     const int c = tid & 15;
     const int rg = tid >> 4;
     // pass-2 mapping: block b of kBlockRows rows, 4-column word w
-    constexpr int kBlockRows = kFastThreads == 256 ? 16 : 8;
-    constexpr int kBlocks = kTileRows / kBlockRows;       // 8 or 16
+    constexpr int kBlockRows = 16;
+    constexpr int kBlocks = kTileRows / kBlockRows;       // 8
     const int b = lane % kBlocks;
     const int w = warp * (32 / kBlocks) + lane / kBlocks;
 
@@ -462,19 +457,10 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
 // dominate: keep as many in flight as possible), 3 stages for long runs
 // (measured on GB300: fewer outstanding tile loads per SM leave DRAM more
 // room for the output writes and sustain a higher read+write rate).
-// Resident CTAs per SM: 1 (compile-time constant).
-#ifndef CT_MINB
-#define CT_MINB 1
-#endif
-constexpr int kMinBlocks = CT_MINB;
-#ifndef CT_STAGES_SHORT
-#define CT_STAGES_SHORT 4
-#endif
-#ifndef CT_STAGES_LONG
-#define CT_STAGES_LONG 3
-#endif
-constexpr int kStagesShort = CT_STAGES_SHORT;
-constexpr int kStagesLong = CT_STAGES_LONG;
+// Resident CTAs per SM: 1 (2 was measured and was slower).
+constexpr int kMinBlocks = 1;
+constexpr int kStagesShort = 4;
+constexpr int kStagesLong = 3;
 constexpr int64_t kLongRunTiles = 16;   // tiles per CTA from which the long setting wins
 
 struct LaunchCache {

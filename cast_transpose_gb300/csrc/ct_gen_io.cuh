@@ -1,10 +1,9 @@
-// ct_gen_io.cuh -- loads and stores of the general kernels for any
-// alignment: 8 bf16 (or 16 bytes) shifted out of the two aligned 16-byte
-// blocks that cover them, and 8- / 16-byte stores as one vector store when
-// aligned, else as aligned 4-byte words shifted across registers plus a 1- to
-// 3-byte head and tail (byte by byte when cut short).  Shared by the general
-// kernels and by the direct-load kernel's transposed stores when rows is not a
-// multiple of 16.
+// ct_gen_io.cuh -- loads and stores for any alignment: 8 bf16 (or 16 bytes)
+// shifted out of the two aligned 16-byte blocks that cover them, and row
+// segments of FP8 codes written as aligned 16-byte blocks whose bytes are
+// gathered from neighbouring lanes (masked only at the two segment ends).
+// Shared by the general kernels and by the direct-load kernel's transposed
+// stores when rows is not a multiple of 16.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -59,8 +58,13 @@ __device__ __forceinline__ uint4 keep_first_bytes(uint4 v, int n) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Word i (0..3) of w, by selects (no indexed access, so w stays in registers).
+__device__ __forceinline__ uint32_t word_of(const uint32_t (&w)[4], int i) {
+    return i == 0 ? w[0] : i == 1 ? w[1] : i == 2 ? w[2] : w[3];
+}
+
 __device__ __forceinline__ uint8_t byte_of(const uint32_t (&w)[4], int i) {
-    return static_cast<uint8_t>(w[i >> 2] >> (8 * (i & 3)));
+    return static_cast<uint8_t>(word_of(w, i >> 2) >> (8 * (i & 3)));
 }
 
 // Store the K words d[0..K-1] (4K bytes) at dst, where h = dst & 3 is 1, 2
@@ -88,32 +92,6 @@ __device__ __forceinline__ void store_words_unaligned(uint8_t* dst, const uint32
     }
 }
 
-// Bytes 0..n-1 of the 16 in w to dst.
-__device__ __forceinline__ void store16(uint8_t* dst, const uint32_t (&w)[4], int n) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(dst);
-    if (n == 16) {
-        if ((a & 15) == 0) {
-            __stcs(reinterpret_cast<uint4*>(dst), make_uint4(w[0], w[1], w[2], w[3]));
-            return;
-        }
-        if ((a & 7) == 0) {
-            __stcs(reinterpret_cast<uint2*>(dst), make_uint2(w[0], w[1]));
-            __stcs(reinterpret_cast<uint2*>(dst + 8), make_uint2(w[2], w[3]));
-            return;
-        }
-        if ((a & 3) == 0) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) reinterpret_cast<uint32_t*>(dst)[j] = w[j];
-            return;
-        }
-        store_words_unaligned<4>(dst, w, static_cast<int>(a & 3));
-        return;
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        if (i < n) dst[i] = byte_of(w, i);
-}
-
 // Bytes 0..n-1 of the 8 in q to dst.
 __device__ __forceinline__ void store8(uint8_t* dst, uint2 q, int n) {
     const uintptr_t a = reinterpret_cast<uintptr_t>(dst);
@@ -135,6 +113,125 @@ __device__ __forceinline__ void store8(uint8_t* dst, uint2 q, int n) {
 #pragma unroll
     for (int i = 0; i < 8; ++i)
         if (i < n) dst[i] = byte_of(w, i);
+}
+
+// ---- row segments written as aligned 16-byte blocks ------------------------
+// A row segment of L <= 128 bytes at any address `seg` is held in registers
+// as 16-byte pieces (piece k = segment bytes [16k, 16k + 16)).  With m =
+// seg & 15, the aligned 16-byte block k (address seg - m + 16k) holds segment
+// bytes [16k - m, 16k - m + 16): the top m bytes of piece k - 1 and the low
+// 16 - m bytes of piece k.  Every block is stored with one 16-byte store
+// except those cut by the segment ends (the first, the last), whose bytes
+// inside the segment are stored in aligned pieces of 8, 4, 2 and 1 bytes;
+// no byte outside the segment is touched.
+
+// Store bytes [lo, hi) of the 16 in w at blk (16-byte aligned), in aligned
+// pieces.
+__device__ __forceinline__ void store_range(uint8_t* blk, const uint32_t (&w)[4], int lo, int hi) {
+    while (lo < hi) {
+        const uint32_t wd = word_of(w, lo >> 2);
+        if ((lo & 7) == 0 && lo + 8 <= hi) {
+            *reinterpret_cast<uint2*>(blk + lo) = make_uint2(wd, word_of(w, (lo >> 2) + 1));
+            lo += 8;
+        } else if ((lo & 3) == 0 && lo + 4 <= hi) {
+            *reinterpret_cast<uint32_t*>(blk + lo) = wd;
+            lo += 4;
+        } else if ((lo & 1) == 0 && lo + 2 <= hi) {
+            *reinterpret_cast<uint16_t*>(blk + lo) = static_cast<uint16_t>(wd >> (8 * (lo & 3)));
+            lo += 2;
+        } else {
+            blk[lo] = static_cast<uint8_t>(wd >> (8 * (lo & 3)));
+            lo += 1;
+        }
+    }
+}
+
+// Block k of a segment (see above), given pieces k - 1 (`prev`, unused for
+// k == 0) and k (`cur`); `last`: also store block k + 1 (the block after the
+// last piece, holding its top m bytes) when the segment reaches into it.
+__device__ __forceinline__ void store_block(uint8_t* seg, int L, int k, const uint32_t (&prev)[4],
+                                            const uint32_t (&cur)[4], bool last) {
+    const int m = static_cast<int>(reinterpret_cast<uintptr_t>(seg) & 15);
+    if (16 * k - m >= L) return;                 // block entirely past the segment end
+    uint8_t* blk = seg - m + 16 * k;
+    if (m == 0) {
+        if (16 * k + 16 <= L) __stcs(reinterpret_cast<uint4*>(blk), make_uint4(cur[0], cur[1], cur[2], cur[3]));
+        else store_range(blk, cur, 0, L - 16 * k);
+        return;
+    }
+    const uint4 v4 = extract16(make_uint4(prev[0], prev[1], prev[2], prev[3]),
+                               make_uint4(cur[0], cur[1], cur[2], cur[3]), 16 - m);
+    const uint32_t v[4] = {v4.x, v4.y, v4.z, v4.w};
+    const int lo = k == 0 ? m : 0;
+    const int hi = min(16, L - 16 * k + m);
+    if (lo == 0 && hi == 16) __stcs(reinterpret_cast<uint4*>(blk), v4);
+    else store_range(blk, v, lo, hi);
+    if (last && L - 16 * k - 16 + m > 0) {      // block k + 1: top m bytes of piece k
+        const uint4 t4 = extract16(make_uint4(cur[0], cur[1], cur[2], cur[3]),
+                                   make_uint4(0u, 0u, 0u, 0u), 16 - m);
+        const uint32_t t[4] = {t4.x, t4.y, t4.z, t4.w};
+        store_range(blk + 16, t, 0, min(16, L - 16 * k - 16 + m));
+    }
+}
+
+// Bytes [lo, 16) (head) or [0, hi) (tail) of the 16 in w at blk (16-byte
+// aligned), 0 < lo, hi < 16: whole words with word stores, the one cut word
+// with a byte and/or a 2-byte store; straight-line predicated code.
+__device__ __forceinline__ void store_head(uint8_t* blk, const uint32_t (&w)[4], int lo) {
+    const int w0 = (lo + 3) >> 2;   // first whole word
+#pragma unroll
+    for (int i = 1; i < 4; ++i)
+        if (i >= w0) reinterpret_cast<uint32_t*>(blk)[i] = w[i];
+    const int r = lo & 3;
+    const uint32_t cut = word_of(w, lo >> 2);
+    uint8_t* cw = blk + (lo & ~3);
+    if (r == 1 || r == 3) cw[r] = static_cast<uint8_t>(cut >> (8 * r));
+    if (r == 1 || r == 2) *reinterpret_cast<uint16_t*>(cw + 2) = static_cast<uint16_t>(cut >> 16);
+}
+__device__ __forceinline__ void store_tail(uint8_t* blk, const uint32_t (&w)[4], int hi) {
+    const int w1 = hi >> 2;         // whole words [0, w1)
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+        if (i < w1) reinterpret_cast<uint32_t*>(blk)[i] = w[i];
+    const int r = hi & 3;
+    const uint32_t cut = word_of(w, w1);
+    uint8_t* cw = blk + 4 * w1;
+    if (r >= 2) *reinterpret_cast<uint16_t*>(cw) = static_cast<uint16_t>(cut);
+    if (r == 1) cw[0] = static_cast<uint8_t>(cut);
+    if (r == 3) cw[2] = static_cast<uint8_t>(cut >> 16);
+}
+
+// Full 128-byte segments (the common case) in aligned blocks: lanes 1..7 of
+// the group store block b, lane 0 the head block (its top 16 - m bytes) and
+// lane 7 also the tail block (the low m bytes of block 8).  Shorter
+// segments go through store_block.
+__device__ __forceinline__ void store_segment_x8(uint8_t* seg, int L, const uint32_t (&w)[4],
+                                                      int b) {
+    uint32_t prev[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) prev[i] = __shfl_up_sync(0xFFFFFFFFu, w[i], 1, 8);
+    if (L <= 0) return;
+    const int m = static_cast<int>(reinterpret_cast<uintptr_t>(seg) & 15);
+    if (L < 128) {
+        store_block(seg, L, b, prev, w, b == 7);
+        return;
+    }
+    uint8_t* blk = seg - m + 16 * b;
+    if (m == 0) {
+        __stcs(reinterpret_cast<uint4*>(blk), make_uint4(w[0], w[1], w[2], w[3]));
+        return;
+    }
+    const uint4 v4 = extract16(make_uint4(prev[0], prev[1], prev[2], prev[3]),
+                               make_uint4(w[0], w[1], w[2], w[3]), 16 - m);
+    const uint32_t v[4] = {v4.x, v4.y, v4.z, v4.w};
+    if (b == 0) store_head(blk, v, m);
+    else __stcs(reinterpret_cast<uint4*>(blk), v4);
+    if (b == 7) {   // block 8: the top m bytes of piece 7
+        const uint4 t4 = extract16(make_uint4(w[0], w[1], w[2], w[3]), make_uint4(0u, 0u, 0u, 0u),
+                                   16 - m);
+        const uint32_t t[4] = {t4.x, t4.y, t4.z, t4.w};
+        store_tail(blk + 16, t, m);
+    }
 }
 
 }  // namespace gen

@@ -20,6 +20,8 @@
 #include <cuda_bf16.h>
 
 #include <cmath>
+#include <mutex>
+
 
 namespace ct {
 namespace {
@@ -28,39 +30,63 @@ namespace {
 // General cast: any shape, x 2-byte aligned, out and out_t 1-byte aligned.
 // Tile 128x128, 256 threads, the thread mapping of the direct-load kernel
 // (pass 1: 8-column chunk c of rows rg + 16*it; pass 2: 16-row x 4-column
-// byte blocks).  Loads and stores take the widest aligned form the address
-// allows, and never touch a byte outside the caller's buffers:
-//   * a row chunk (8 elements) is one 16-byte load when it is 16-byte
-//     aligned; otherwise the two aligned 16-byte blocks that cover it are
-//     loaded when both lie inside x, and the 8 elements are shifted out of
-//     them in registers; otherwise (the first and last blocks of x) the
-//     elements are loaded one by one;
-//   * elements past the end of the row read as zero (they belong to the next
-//     row) and are neither stored nor counted;
-//   * q chunks (8 bytes) and qT blocks (16 bytes) are stored with one vector
-//     store when aligned, else as aligned 4-byte words shifted across
-//     registers plus a 1- to 3-byte head and tail; chunks cut short by the
-//     matrix edge are stored byte by byte (helpers in ct_gen_io.cuh).
+// byte blocks).  No byte outside the caller's buffers is touched:
+//   * staging: the segment of each tile row in x (up to 256 bytes starting
+//     at any even byte) is copied into shared memory as the aligned 16-byte
+//     chunks that cover it, up to 17, with cp.async (nothing held in
+//     registers while the copies are in flight); a chunk
+//     that crosses the end of x copies only the bytes up to it, and the one
+//     chunk that can start before x (its first) is read element by element;
+//   * pass 1: the 8 elements of chunk c come out of two staged chunks by a
+//     register shift; amax, column sums and cast as in the direct kernel;
+//     elements past the row end are zeroed (they belong to the next row);
+//     q is stored 8 bytes per thread, as aligned words shifted across
+//     registers plus a short head and tail where the address is not aligned
+//     (gen::store8);
+//   * pass 2: the transposed 16-row blocks; when rows is a multiple of 16
+//     and out_t is 16-byte aligned every block is one aligned 16-byte store,
+//     otherwise each column's segment of qT is written as aligned 16-byte
+//     blocks gathered from neighbouring lanes (gen::store_segment_x8).
+// Measured on GB300 (8191x12287, both dimensions odd): 3.24 TB/s, limited by
+// instruction issue (79% of scheduler cycles issue; DRAM 36% busy): the
+// shifts and partial stores that misalignment costs.  Aligned-block stores
+// for both q and qT with the end blocks written by a loop ran at 1.63 TB/s;
+// per-thread unaligned 16-byte stores of qT at 2.98 TB/s.
+constexpr int kStageRow = 17 * 16;   // staged bytes per tile row
+constexpr int kGenSmem = kTileRows * kStageRow + kTileRows * kTileCols;
+constexpr int kGenSmemDbias = kGenSmem + 8 * dev::kColsumStride * 4;
 
-// Rows of a thread's 8 loaded per batch, and resident CTAs per SM.  Measured
-// on GB300 (odd rows and cols / x shifted by 2 bytes / cols % 16 = 8): batches
-// of 8 at 2 CTAs per SM 2.65 / 3.83 / 4.40 TB/s, batches of 4 at 4 CTAs per
-// SM (64 registers) 3.08 / 5.04 / 5.34 TB/s.
-#ifndef CT_GEN_BATCH
-#define CT_GEN_BATCH 4
-#endif
-#ifndef CT_GEN_MINB
-#define CT_GEN_MINB 4
-#endif
-constexpr int kGenBatch = CT_GEN_BATCH;
+// One 16-byte staging chunk of x at src (16-byte aligned) into dst, if it
+// holds bytes of the row segment that ends at send: a cp.async for the bytes
+// inside x, or element loads for the first chunk of x when it starts before
+// x.
+__device__ __forceinline__ void stage_chunk(uint8_t* dst, uintptr_t src, uintptr_t send,
+                                            uintptr_t xbeg, uintptr_t xend) {
+    if (src >= send) return;   // past the segment
+    if (src < xbeg) {
+        uint32_t e[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uintptr_t ad = src + 2 * i;
+            if (ad >= xbeg && ad < xend)
+                e[i >> 1] |= uint32_t(*reinterpret_cast<const uint16_t*>(ad)) << (16 * (i & 1));
+        }
+        *reinterpret_cast<uint4*>(dst) = make_uint4(e[0], e[1], e[2], e[3]);
+        return;
+    }
+    const uintptr_t left = xend - src;   // > 0: src is inside the segment
+    dev::cp_async16(dst, reinterpret_cast<const void*>(src), left < 16 ? static_cast<int>(left) : 16);
+}
 
 template <int FMT, bool DBIAS>
-__global__ void __launch_bounds__(256, CT_GEN_MINB) general_cast_kernel(GeneralArgs a) {
+__global__ void __launch_bounds__(256, DBIAS ? 3 : 4) general_cast_kernel(GeneralArgs a) {
     dev::pdl_launch_dependents();
     dev::pdl_wait();
     if (a.noop != nullptr && *a.noop != 0.0f) return;
-    __shared__ __align__(16) uint8_t sq[kTileRows * kTileCols];
-    __shared__ __align__(16) float colsum[8 * kTileCols];
+    extern __shared__ __align__(16) uint8_t gsmem[];
+    uint8_t* xs = gsmem;                                   // [128][kStageRow]
+    uint8_t* sq = gsmem + kTileRows * kStageRow;           // swizzled FP8 copy
+    float* colsum = reinterpret_cast<float*>(sq + kTileRows * kTileCols);
     __shared__ unsigned s_amax[8];
 
     const int64_t rows = a.rows, cols = a.cols;
@@ -76,85 +102,66 @@ __global__ void __launch_bounds__(256, CT_GEN_MINB) general_cast_kernel(GeneralA
     for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
         const int64_t rt = tile / tiles_c;
         const int64_t row0 = rt * kTileRows, col0 = (tile - rt * tiles_c) * kTileCols;
-        const int64_t ccol = col0 + 8 * c;
-        const int nv = ccol >= cols ? 0 : (cols - ccol >= 8 ? 8 : static_cast<int>(cols - ccol));
+        const int nrow = static_cast<int>(rows - row0 < kTileRows ? rows - row0 : kTileRows);
+        const int ncol = static_cast<int>(cols - col0 < kTileCols ? cols - col0 : kTileCols);
 
+        // ---- staging of the tile's row segments: consecutive threads on
+        // consecutive chunks (17 per row), so each copy instruction of a warp
+        // covers about two rows of contiguous chunks ----
+        for (int i = tid; i < kTileRows * 17; i += 256) {
+            const int r = i / 17, u = i - 17 * r;
+            if (r >= nrow) break;
+            const uintptr_t s0 = xbeg + 2 * uintptr_t((row0 + r) * cols + col0);
+            stage_chunk(xs + r * kStageRow + 16 * u, (s0 & ~uintptr_t(15)) + 16 * uintptr_t(u),
+                        s0 + 2 * uintptr_t(ncol), xbeg, xend);
+        }
+        dev::cp_async_wait_all();
+        __syncthreads();
+
+        // ---- pass 1: amax, column sums, cast, q and the FP8 copy ----
         uint32_t amax_pair = 0;
         float cs[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) cs[j] = 0.0f;
-#pragma unroll
-        for (int it0 = 0; it0 < 8; it0 += kGenBatch) {
-            // ---- loads of the batch: all issued before any use ----
-            uint4 lo[kGenBatch], hi[kGenBatch];
-            int mode[kGenBatch];   // 0 none, 1 aligned, 2 two aligned blocks, 3 element-wise
-#pragma unroll
-            for (int u = 0; u < kGenBatch; ++u) {
-                const int64_t row = row0 + rg + 16 * (it0 + u);
-                const int n = row < rows ? nv : 0;
-                const uint16_t* src = a.x + row * cols + ccol;
-                const uintptr_t ad = reinterpret_cast<uintptr_t>(src);
-                const uintptr_t b0 = ad & ~uintptr_t(15);
-                lo[u] = make_uint4(0u, 0u, 0u, 0u);
-                hi[u] = lo[u];
-                mode[u] = 0;
-                if (n > 0) {
-                    if (b0 == ad && b0 + 16 <= xend) {
-                        lo[u] = __ldcs(reinterpret_cast<const uint4*>(b0));
-                        mode[u] = 1;
-                    } else if (b0 >= xbeg && b0 + 32 <= xend) {
-                        lo[u] = __ldcs(reinterpret_cast<const uint4*>(b0));
-                        hi[u] = __ldcs(reinterpret_cast<const uint4*>(b0 + 16));
-                        mode[u] = 2;
-                    } else {
-                        uint32_t e[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            if (i < n) e[i >> 1] |= uint32_t(__ldcs(src + i)) << (16 * (i & 1));
-                        lo[u] = make_uint4(e[0], e[1], e[2], e[3]);
-                        mode[u] = 3;
-                    }
-                }
-            }
-
-            // ---- pass 1: amax, column sums, cast, q and the FP8 copy ----
-#pragma unroll
-            for (int u = 0; u < kGenBatch; ++u) {
-                const int r = rg + 16 * (it0 + u);
-                const int64_t row = row0 + r;
-                const int n = row < rows ? nv : 0;
-                uint4 v = mode[u] == 2
-                              ? gen::extract8(lo[u], hi[u],
-                                              static_cast<int>((reinterpret_cast<uintptr_t>(
-                                                                    a.x + row * cols + ccol) &
-                                                                15) >> 1))
-                              : lo[u];
+        const int nv = ncol - 8 * c <= 0 ? 0 : (ncol - 8 * c >= 8 ? 8 : ncol - 8 * c);
+        // byte offset in x of this thread's first row segment, and its step
+        uint32_t xoff = static_cast<uint32_t>(
+            (xbeg + 2 * uintptr_t((row0 + rg) * cols + col0)) & 15);
+        const uint32_t xstep = static_cast<uint32_t>((32 * uintptr_t(cols)) & 15);
+#pragma unroll 2
+        for (int it = 0; it < 8; ++it) {
+            const int r = rg + 16 * it;
+            const int64_t row = row0 + r;
+            const int n = r < nrow ? nv : 0;
+            const int mx = static_cast<int>(xoff);
+            xoff = (xoff + xstep) & 15;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (n > 0) {
+                const uint8_t* rp = xs + r * kStageRow + 16 * c;
+                v = *reinterpret_cast<const uint4*>(rp);
+                if (mx != 0) v = gen::extract8(v, *reinterpret_cast<const uint4*>(rp + 16), mx >> 1);
                 if (n < 8) v = gen::keep_first(v, n);
-                amax_pair = dev::absmax_pair(amax_pair, v.x);
-                amax_pair = dev::absmax_pair(amax_pair, v.y);
-                amax_pair = dev::absmax_pair(amax_pair, v.z);
-                amax_pair = dev::absmax_pair(amax_pair, v.w);
-                if constexpr (DBIAS) {
-                    cs[0] += dev::bf16_lo(v.x); cs[1] += dev::bf16_hi(v.x);
-                    cs[2] += dev::bf16_lo(v.y); cs[3] += dev::bf16_hi(v.y);
-                    cs[4] += dev::bf16_lo(v.z); cs[5] += dev::bf16_hi(v.z);
-                    cs[6] += dev::bf16_lo(v.w); cs[7] += dev::bf16_hi(v.w);
-                }
-                const uint2 q8 = dev::cast8<FMT>(v, scale);
-                if (a.out != nullptr && n > 0) gen::store8(a.out + row * cols + ccol, q8, n);
-                *reinterpret_cast<uint2*>(sq + r * kTileCols + ((2 * c) ^ dev::swz(r)) * 4) = q8;
             }
+            amax_pair = dev::absmax_pair(amax_pair, v.x);
+            amax_pair = dev::absmax_pair(amax_pair, v.y);
+            amax_pair = dev::absmax_pair(amax_pair, v.z);
+            amax_pair = dev::absmax_pair(amax_pair, v.w);
+            if constexpr (DBIAS) {
+                cs[0] += dev::bf16_lo(v.x); cs[1] += dev::bf16_hi(v.x);
+                cs[2] += dev::bf16_lo(v.y); cs[3] += dev::bf16_hi(v.y);
+                cs[4] += dev::bf16_lo(v.z); cs[5] += dev::bf16_hi(v.z);
+                cs[6] += dev::bf16_lo(v.w); cs[7] += dev::bf16_hi(v.w);
+            }
+            const uint2 q8 = dev::cast8<FMT>(v, scale);
+            if (a.out != nullptr && n > 0) gen::store8(a.out + row * cols + col0 + 8 * c, q8, n);
+            *reinterpret_cast<uint2*>(sq + r * kTileCols + ((2 * c) ^ dev::swz(r)) * 4) = q8;
         }
         const unsigned m = __reduce_max_sync(0xFFFFFFFFu, dev::pair_to_f32_bits(amax_pair));
         if (lane == 0) s_amax[warp] = m;
         if constexpr (DBIAS) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) cs[j] += __shfl_xor_sync(0xFFFFFFFFu, cs[j], 16);
-            if (lane < 16) {
-                float4* dst = reinterpret_cast<float4*>(colsum + warp * kTileCols + 8 * c);
-                dst[0] = make_float4(cs[0], cs[1], cs[2], cs[3]);
-                dst[1] = make_float4(cs[4], cs[5], cs[6], cs[7]);
-            }
+            if (lane < 16) dev::colsum_store(colsum, warp, c, cs);
         }
         __syncthreads();
 
@@ -167,9 +174,9 @@ __global__ void __launch_bounds__(256, CT_GEN_MINB) general_cast_kernel(GeneralA
         }
         if constexpr (DBIAS) {
             if (tid < kTileCols && col0 + tid < cols) {
-                float sum = colsum[tid];
+                float sum = colsum[dev::colsum_index(0, tid)];
 #pragma unroll
-                for (int j = 1; j < 8; ++j) sum += colsum[j * kTileCols + tid];
+                for (int j = 1; j < 8; ++j) sum += colsum[dev::colsum_index(j, tid)];
                 a.partial[rt * cols + col0 + tid] = sum;
             }
         }
@@ -188,40 +195,36 @@ __global__ void __launch_bounds__(256, CT_GEN_MINB) general_cast_kernel(GeneralA
             for (int g = 0; g < 4; ++g)
                 dev::transpose4x4(rw[4 * g], rw[4 * g + 1], rw[4 * g + 2], rw[4 * g + 3], o[0][g],
                                   o[1][g], o[2][g], o[3][g]);
-            const int64_t row = row0 + 16 * b;
-            const int nr = row >= rows ? 0 : (rows - row >= 16 ? 16 : static_cast<int>(rows - row));
-            if (nr > 0) {
+            if ((rows & 15) == 0 && (reinterpret_cast<uintptr_t>(a.out_t) & 15) == 0) {
+                // every column's segment of qT starts on a 16-byte boundary
+                if (16 * b < nrow) {
+#pragma unroll
+                    for (int kq = 0; kq < 4; ++kq) {
+                        const int64_t col = col0 + 4 * w + kq;
+                        if (col < cols)
+                            __stcs(reinterpret_cast<uint4*>(a.out_t + col * rows + row0 + 16 * b),
+                                   make_uint4(o[kq][0], o[kq][1], o[kq][2], o[kq][3]));
+                    }
+                }
+            } else {
 #pragma unroll
                 for (int kq = 0; kq < 4; ++kq) {
                     const int64_t col = col0 + 4 * w + kq;
-                    if (col < cols) gen::store16(a.out_t + col * rows + row, o[kq], nr);
+                    gen::store_segment_x8(a.out_t + col * rows + row0, col < cols ? nrow : 0, o[kq], b);
                 }
             }
         }
-        __syncthreads();   // sq, colsum and s_amax are reused by the next tile
+        __syncthreads();   // the staging, sq, colsum and s_amax are reused by the next tile
     }
 }
 
 // ---------------------------------------------------------------------------
 // db[j] = sum over the `runs` partial rows of partial[t, j] (one row per
 // band of tile rows, see dbias_units).  Block = 32 columns x 8 row groups;
-// each thread sums every 8th partial row of its column, then the 8 group
-// sums are added in a fixed order (deterministic).  The sums are
-// compensated (Kahan) fp32: the error stays within a few fp32 ulps of the sum
-// of magnitudes for any number of row tiles, without fp64 arithmetic, which
-// runs at a small fraction of the fp32 rate on this GPU.
-// Once the sum is not finite (an Inf or NaN in the column) the compensation
-// is dropped, so the sum keeps the plain IEEE result (Inf, or NaN for
-// Inf - Inf and NaN inputs) instead of the Inf - Inf of the correction term.
-struct Kahan {
-    float sum = 0.0f, comp = 0.0f;
-    __device__ __forceinline__ void add(float v) {
-        const float y = __fsub_rn(v, comp);
-        const float t = __fadd_rn(sum, y);
-        comp = isfinite(t) ? __fsub_rn(__fsub_rn(t, sum), y) : 0.0f;
-        sum = t;
-    }
-};
+// each thread sums every 8th partial row of its column (its loads for 64
+// rows issued together, one round trip to L2), then the 8 group sums are
+// added in a fixed order (deterministic), all compensated (dev::Kahan).
+using dev::Kahan;
 
 template <bool BF16_OUT>
 __global__ void __launch_bounds__(256) dbias_finish_kernel(const float* __restrict__ partial,
@@ -237,9 +240,18 @@ __global__ void __launch_bounds__(256) dbias_finish_kernel(const float* __restri
     for (int64_t col0 = int64_t(blockIdx.x) * 32; col0 < cols; col0 += int64_t(gridDim.x) * 32) {
         const int64_t j = col0 + c;
         Kahan k;
-        if (j < cols) {
-#pragma unroll 4
-            for (int64_t t = g; t < runs; t += 8) k.add(partial[t * cols + j]);
+        if (j < cols) {   // eight rows per thread per batch, all loads issued first
+            for (int64_t t0 = 0; t0 < runs; t0 += 64) {
+                float v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int64_t t = t0 + g + 8 * i;
+                    v[i] = t < runs ? __ldcg(partial + t * cols + j) : 0.0f;
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (t0 + g + 8 * i < runs) k.add(v[i]);
+            }
         }
         part[g][c] = k.sum;
         comp[g][c] = k.comp;
@@ -363,7 +375,7 @@ __global__ void __launch_bounds__(256) transpose_fast_kernel(const uint8_t* __re
 // load, else the two aligned blocks covering it (both inside `in`) shifted in
 // registers, else byte loads (first and last blocks of `in` only); bytes past
 // the row end are zeroed.  The transposed 16-byte blocks are stored with
-// gen::store16.
+// gen::store_segment_x8 (aligned 16-byte blocks, masked at the segment ends).
 __global__ void __launch_bounds__(256) transpose_general_kernel(const uint8_t* __restrict__ in,
                                                                 int64_t rows, int64_t cols,
                                                                 uint8_t* __restrict__ out,
@@ -440,14 +452,11 @@ __global__ void __launch_bounds__(256) transpose_general_kernel(const uint8_t* _
         for (int g = 0; g < 4; ++g)
             dev::transpose4x4(rw[4 * g], rw[4 * g + 1], rw[4 * g + 2], rw[4 * g + 3], o[0][g],
                               o[1][g], o[2][g], o[3][g]);
-        const int64_t row = row0 + 16 * b;
-        const int nr = row >= rows ? 0 : (rows - row >= 16 ? 16 : static_cast<int>(rows - row));
-        if (nr > 0) {
+        const int nrow = static_cast<int>(rows - row0 < kTileRows ? rows - row0 : kTileRows);
 #pragma unroll
-            for (int kq = 0; kq < 4; ++kq) {
-                const int64_t col = col0 + 4 * w + kq;
-                if (col < cols) gen::store16(out + col * rows + row, o[kq], nr);
-            }
+        for (int kq = 0; kq < 4; ++kq) {
+            const int64_t col = col0 + 4 * w + kq;
+            gen::store_segment_x8(out + col * rows + row0, col < cols ? nrow : 0, o[kq], b);
         }
         __syncthreads();
     }
@@ -479,18 +488,47 @@ unsigned grid_for(int64_t tiles, int64_t cap) {
     return static_cast<unsigned>(tiles < cap ? tiles : cap);
 }
 
+// The general kernel's dynamic shared memory is above the default 48 KB
+// limit: raise it once per device and variant.
+template <int FMT, bool DBIAS>
+cudaError_t general_smem_attr() {
+    static std::mutex mu;
+    static bool done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done[dev]) {
+        e = cudaFuncSetAttribute(general_cast_kernel<FMT, DBIAS>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 DBIAS ? kGenSmemDbias : kGenSmem);
+        if (e != cudaSuccess) return e;
+        done[dev] = true;
+    }
+    return cudaSuccess;
+}
+
+template <int FMT, bool DBIAS>
+cudaError_t launch_general_t(const GeneralArgs& a, dim3 grid, cudaStream_t stream) {
+    const cudaError_t e = general_smem_attr<FMT, DBIAS>();
+    if (e != cudaSuccess) return e;
+    return launch_pdl(general_cast_kernel<FMT, DBIAS>, grid, dim3(256),
+                      DBIAS ? kGenSmemDbias : kGenSmem, stream, a);
+}
+
 }  // namespace
 
 cudaError_t launch_general(const GeneralArgs& a, int fmt, cudaStream_t stream) {
     const int64_t tiles =
         ((a.rows + kTileRows - 1) / kTileRows) * ((a.cols + kTileCols - 1) / kTileCols);
-    const dim3 grid(grid_for(tiles, int64_t(1) << 30)), block(256);
+    const dim3 grid(grid_for(tiles, int64_t(1) << 30));
     const bool dbias = a.partial != nullptr;
     if (fmt == 0)
-        return dbias ? launch_pdl(general_cast_kernel<0, true>, grid, block, 0, stream, a)
-                     : launch_pdl(general_cast_kernel<0, false>, grid, block, 0, stream, a);
-    return dbias ? launch_pdl(general_cast_kernel<1, true>, grid, block, 0, stream, a)
-                 : launch_pdl(general_cast_kernel<1, false>, grid, block, 0, stream, a);
+        return dbias ? launch_general_t<0, true>(a, grid, stream)
+                     : launch_general_t<0, false>(a, grid, stream);
+    return dbias ? launch_general_t<1, true>(a, grid, stream)
+                 : launch_general_t<1, false>(a, grid, stream);
 }
 
 cudaError_t launch_dbias_finish(const float* partial, int64_t runs, int64_t cols, void* dbias,

@@ -109,10 +109,7 @@ struct DirectParams {
     const float* noop;      // nullable device flag
     float* partial;         // dbias partials [ceil(rows/128), cols] (one row per tile row), or null
 };
-#ifndef CT_DIRECT_MIN_TILES
-#define CT_DIRECT_MIN_TILES 2048
-#endif
-constexpr int64_t kDirectMinTiles = CT_DIRECT_MIN_TILES;
+constexpr int64_t kDirectMinTiles = 2048;
 // `variant`: 0 = cast + transpose, 1 = cast only; `dbias` requires variant 0.
 cudaError_t launch_direct(const DirectParams<1>& p, int fmt, bool dbias, int variant,
                           cudaStream_t stream);
@@ -145,10 +142,7 @@ __host__ __device__ __forceinline__ DbiasUnits dbias_units(int64_t R, int64_t H)
 }
 // Band height: 4 measured best on GB300 (shorter bands balance the last
 // wave of units better, longer ones write fewer partial rows).
-#ifndef CT_DBIAS_BAND
-#define CT_DBIAS_BAND 4
-#endif
-constexpr int64_t kDbiasBand = CT_DBIAS_BAND;
+constexpr int64_t kDbiasBand = 4;
 
 // Dbias finish: db[j] = sum of the `runs` partial rows (compensated fp32),
 // stored as fp32, or (db_bf16) rounded to bf16, nearest even.

@@ -193,3 +193,47 @@ def test_gradient_8192x12288_bf16_db_two_steps():
         hist, s_arr, _ = oracle.amax_and_scale_update(hist, np.float32([s_val]), np.ones(1, np.float32),
                                                       ct.E5M2, 0)
         s_val = float(s_arr[0])
+
+
+@pytest.mark.parametrize("shape", [(4096, 8192), (4095, 4096)])
+def test_graph_replays_with_new_data_and_a_shared_workspace(shape):
+    """The per-tile column sums live in the workspace between the two kernels
+    of a call; a replay of a captured call must add only its own sums, never
+    a previous replay's.  Three replays with different data in the same
+    (captured) buffers, each compared with the oracle; then another shape
+    through the same workspace."""
+    rows, cols = shape
+    dy = torch.empty(rows, cols, dtype=torch.bfloat16, device="cuda")
+    q, qt = ct.empty_outputs(dy)
+    db = torch.empty(cols, device="cuda")
+    ws = torch.empty(ct.dbias_workspace_size(rows, cols), dtype=torch.uint8, device="cuda")
+    s, a, si = scalar(1.0), scalar(0.0), scalar(0.0)
+    dy.copy_(workloads.normal_bf16(rows, cols, 1.0, 900, "cuda"))
+    ct.fp8_dbias_cast_transpose(dy, s, a, si, q, qt, db, ws, ct.E5M2)   # eager warm-up
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side), torch.cuda.graph(g):
+        ct.fp8_dbias_cast_transpose(dy, s, a, si, q, qt, db, ws, ct.E5M2)
+    torch.cuda.current_stream().wait_stream(side)
+    for rep in range(3):
+        x_cpu = workloads.normal_bf16(rows, cols, 0.5 + rep, 901 + rep)
+        dy.copy_(x_cpu)
+        a.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert dbias_tolerance_ok(db.cpu().numpy(), oracle.dbias(x_cpu), x_cpu), rep
+        ref = oracle.cast_transpose(x_cpu, 1.0, ct.E5M2)
+        assert np.array_equal(q.cpu().numpy(), ref["q"]), rep
+        assert f32_bits(a.item()) == f32_bits(ref["amax"]), rep
+    # another shape (direct path too: rows % 16 != 0) through the same workspace
+    x2 = workloads.normal_bf16(1001, 2048, 3.0, 950)
+    dy2 = x2.cuda()
+    q2, qt2 = ct.empty_outputs(dy2)
+    db2 = torch.empty(2048, device="cuda")
+    a2, si2 = scalar(0.0), scalar(0.0)
+    ct.fp8_dbias_cast_transpose(dy2, scalar(2.0), a2, si2, q2, qt2, db2, ws, ct.E4M3)
+    torch.cuda.synchronize()
+    check({"q": q2.cpu().numpy(), "qt": qt2.cpu().numpy(), "db": db2.cpu().numpy(),
+           "amax": a2.item(), "scale_inv": si2.item()}, x2, 2.0, ct.E4M3)
