@@ -949,7 +949,10 @@ def profile_case(name: str) -> None:
       'general':    cast-transpose of a ragged 8191x12287 matrix, then three
                     FP8 transposes of its q (the general kernels);
       'noop':       three launches of the activation cast-transpose with the
-                    noop flag set."""
+                    noop flag set;
+      'weight':     three steps of the weight-like 4096x4096 workload (eight
+                    casts of x * 2^k with CT_X_READY, each followed by the
+                    scale update), the persistent TMA kernel."""
     import torch
 
     import cast_transpose_gb300 as ct
@@ -993,6 +996,18 @@ def profile_case(name: str) -> None:
         flag = torch.full((1,), 1.0 if name == "noop" else 0.0, device=dev)
         for _ in range(3):
             ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3, noop_flag=flag)
+    elif name == "weight":
+        base = workloads.weight_matrix(dev)
+        xs = [workloads.weight_rescaled(base, k) for k in workloads.WEIGHT_EXPONENTS]
+        outs = [ct.empty_outputs(x) for x in xs]
+        hist = torch.zeros(HIST_LEN, 1, device=dev)
+        scale, rsinv = torch.ones(1, device=dev), torch.ones(1, device=dev)
+        tsinv = torch.zeros(len(xs), device=dev)
+        for _ in range(3):
+            for k, x in enumerate(xs):
+                ct.fp8_cast_transpose(x, scale, hist[0], tsinv[k:k + 1], outs[k][0], outs[k][1],
+                                      ct.E4M3, x_ready=True)
+                ct.fp8_amax_and_scale_update(hist, scale, rsinv, ct.E4M3, 0)
     elif name == "gradient":
         dy = workloads.gradient_matrix(dev)
         q, qt = ct.empty_outputs(dy)
@@ -1017,7 +1032,8 @@ def _parse(argv=None):
     ap.add_argument("--extra", action=argparse.BooleanOptionalAction, default=True,
                     help="also time the secondary workloads")
     ap.add_argument("--profile-case",
-                    choices=["activation", "gradient", "list", "cast", "general", "noop"],
+                    choices=["activation", "gradient", "list", "cast", "general", "noop",
+                             "weight"],
                     default=None,
                     help="only run 3 launches of one workload's kernel (for ncu) and exit")
     return ap.parse_args(argv)

@@ -2,13 +2,15 @@
 //
 // fp8_dbias_cast_transpose needs a device workspace for its per-tile column
 // partial sums, and the caller provides it.  Some callers have no way to get
-// one: code that runs while a CUDA graph is being captured (where cudaMalloc
-// is not allowed), code called from inside a memory allocator or a memory
-// pool callback (where allocating again would recurse or deadlock), and
-// runtimes that reserve all device memory up front and hand out nothing
+// one where they call it: code called from inside a memory allocator or a
+// memory-pool callback (where allocating again would recurse or deadlock),
+// and runtimes that reserve all device memory up front and hand out nothing
 // more.  This entry point serves them: its scratch is a fixed array in the
 // library's own device memory, reserved when the library is loaded on a GPU
 // and held until the process exits, so the call itself allocates nothing.
+// The array's address is looked up once per device and kept; after a
+// cudaDeviceReset the module is loaded again elsewhere, so the entry point
+// is not to be used on that device again.
 #include "../../include/cast_transpose.h"
 #include "ct_internal.h"
 

@@ -309,25 +309,27 @@ int fp8_cast(const void* x, int64_t rows, int64_t cols, const float* scale,
  * fp8_dbias_cast_transpose_noalloc -- fp8_dbias_cast_transpose without a
  * caller-provided workspace.  The pages have no counterpart to this entry
  * point: it exists for callers that cannot allocate device memory at the
- * point of the call -- code running while a CUDA graph is captured (where
- * cudaMalloc is not allowed), code called from inside an allocator or memory
- * pool (where allocating again would recurse or deadlock), and runtimes that
- * reserve all device memory up front.
+ * point of the call -- code called from inside an allocator or a memory pool
+ * (where allocating again would recurse or deadlock), and runtimes that
+ * reserve all device memory up front and hand none out later.
  *
  *   dy, scale, amax, scale_inv, out, out_t, dbias, fmt, noop_flag, stream:
  *              exactly as in fp8_dbias_cast_transpose
  *
- * Scratch: a fixed 4 MiB array inside the library's device memory (every
- * GPU that loads the library holds it until the process exits).  The call
- * itself allocates nothing: no cudaMalloc, no cudaFree, no allocating
- * library routine.  Limit: fp8_dbias_cast_transpose_workspace_size(rows,
- * cols) <= 4 MiB, i.e. ceil(rows/128) * cols <= 1,048,576 (8192 x 16384,
- * say); larger shapes return CT_ERR_WORKSPACE without launching anything.
- * The first call on each device looks up the array's device address (once,
- * with that device current), so make that first call before any stream
- * capture.  All calls share the one array and nothing in it needs clearing,
- * but calls whose kernels overlap on the GPU (different streams, or several
- * threads) race on it: run them one after another.
+ * Scratch: a fixed 4 MiB array inside the library's device memory (every GPU
+ * that loads the library holds it until the process exits).  The call itself
+ * allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * routine.  Limit: fp8_dbias_cast_transpose_workspace_size(rows, cols) <=
+ * 4 MiB, i.e. ceil(rows/128) * cols <= 1,048,576 (8192 x 16384, say); larger
+ * shapes return CT_ERR_WORKSPACE without launching anything.  The first call
+ * on each device looks up the array's device address (once, with that device
+ * current) and keeps it for the life of the process, so make that first call
+ * before any stream capture, and do not call it again on a device after
+ * cudaDeviceReset.  All calls share the one array, which keeps the last
+ * call's contents; nothing in it has to start at zero (each call reads back
+ * only the partial sums it wrote itself), but calls whose kernels overlap on
+ * the GPU (different streams, or several threads) race on it: run them one
+ * after another.
  * Errors: as fp8_dbias_cast_transpose, plus CT_ERR_WORKSPACE for too large
  * a shape and CT_ERR_CUDA if the address lookup fails.
  */
