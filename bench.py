@@ -672,6 +672,13 @@ def secondary(dev, peaks, args) -> dict:
     res["dbias_cast_transpose 8192x12288 E5M2"] = _rate_entry(
         ms, best, 4 * dy.numel() + 4 * dy.shape[1] + 12, peaks,
         "direct_cast_transpose_kernel (dbias) + dbias_finish_kernel")
+    # the same with the CT_X_READY promise for dy (it holds here: nothing writes dy)
+    ms, best = _timed(torch, lambda: ct.fp8_dbias_cast_transpose(dy, s1, a0, si0, q, qt, db, ws,
+                                                                 ct.E5M2, x_ready=True))
+    res["dbias_cast_transpose 8192x12288 E5M2, CT_DBIAS_X_READY"] = _rate_entry(
+        ms, best, 4 * dy.numel() + 4 * dy.shape[1] + 12, peaks,
+        "direct_cast_transpose_kernel (dbias) + dbias_finish_kernel; the first tiles of dy are "
+        "loaded while the previous call's finish kernel runs (nothing writes dy)")
     del dy, q, qt, db, ws
     # activation 16384x12288: cast-transpose, the launch with the noop flag set,
     # cast only, FP8 transpose
@@ -682,6 +689,12 @@ def secondary(dev, peaks, args) -> dict:
                                                            noop_flag=flag))
     res["cast_transpose 16384x12288 E4M3, noop flag 0"] = _rate_entry(
         ms, best, 4 * x.numel() + 12, peaks, "direct_cast_transpose_kernel")
+    ms, best = _timed(torch, lambda: ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3,
+                                                           x_ready=True))
+    res["cast_transpose 16384x12288 E4M3, CT_X_READY"] = _rate_entry(
+        ms, best, 4 * x.numel() + 12, peaks,
+        "direct_cast_transpose_kernel; the first tiles are loaded while the previous launch ends "
+        "(nothing writes x)")
     flag.fill_(1.0)
     ms, best = _timed(torch, lambda: ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3,
                                                            noop_flag=flag), per_graph=50)

@@ -31,6 +31,7 @@ E4M3 = 0
 E5M2 = 1
 X_READY = 1          # fp8_cast_transpose_ex flag CT_X_READY
 DBIAS_FP32, DBIAS_BF16 = 0, 1   # fp8_dbias_cast_transpose_ex db element types
+DBIAS_X_READY = 0x100           # ... OR'd with the CT_X_READY promise for dy
 FP8_MAX = {E4M3: 448.0, E5M2: 57344.0}
 TORCH_FP8 = {E4M3: torch.float8_e4m3fn, E5M2: torch.float8_e5m2}
 
@@ -176,9 +177,10 @@ def dbias_workspace_size(rows: int, cols: int) -> int:
 
 
 def fp8_dbias_cast_transpose(dy, scale, amax, scale_inv, out, out_t, dbias, workspace,
-                             fmt=E5M2, noop_flag=None, stream=None) -> None:
-    """dbias: fp32 or bf16 [cols]; a bf16 dbias calls fp8_dbias_cast_transpose_ex
-    with CT_DBIAS_BF16."""
+                             fmt=E5M2, noop_flag=None, stream=None, x_ready=False) -> None:
+    """dbias: fp32 or bf16 [cols]; a bf16 dbias, or x_ready=True (the
+    CT_X_READY promise for dy: no kernel still running when this call starts
+    writes it), calls fp8_dbias_cast_transpose_ex."""
     rows, cols = _rc(dy)
     n = rows * cols
     ws = _dev(workspace, "workspace", torch.uint8)
@@ -187,8 +189,10 @@ def fp8_dbias_cast_transpose(dy, scale, amax, scale_inv, out, out_t, dbias, work
             _dev(amax, "amax", torch.float32, 1), _dev(scale_inv, "scale_inv", torch.float32, 1),
             _dev(out, "out", _U8, n), _dev(out_t, "out_t", _U8, n), db)
     tail = (ws, workspace.numel(), fmt, _opt(noop_flag, "noop_flag"), _stream(stream))
-    if dbias.dtype == torch.bfloat16:
-        _check(lib().fp8_dbias_cast_transpose_ex(*head, DBIAS_BF16, *tail))
+    if dbias.dtype == torch.bfloat16 or x_ready:
+        kind = (DBIAS_BF16 if dbias.dtype == torch.bfloat16 else DBIAS_FP32) | \
+               (DBIAS_X_READY if x_ready else 0)
+        _check(lib().fp8_dbias_cast_transpose_ex(*head, kind, *tail))
     else:
         _check(lib().fp8_dbias_cast_transpose(*head, *tail))
 

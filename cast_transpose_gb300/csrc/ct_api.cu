@@ -142,7 +142,8 @@ void fill_tensor(FastTensor& t, const void* out, const void* out_t, const float*
 
 // `runs_out` (dbias only): the number of partial rows the launched kernel
 // writes per column (one per band of tile rows on the TMA path, one per tile
-// row on the direct and general paths).  `x_ready`: CT_X_READY (TMA path).
+// row on the direct and general paths).  `x_ready`: CT_X_READY (TMA and
+// direct paths).
 int cast_impl(const void* x, int64_t rows, int64_t cols, const float* scale, float* amax,
               float* scale_inv, void* out, void* out_t, float* partial, int fmt,
               const float* noop, cudaStream_t stream, int64_t* runs_out = nullptr,
@@ -160,6 +161,7 @@ int cast_impl(const void* x, int64_t rows, int64_t cols, const float* scale, flo
             d.total_tiles = tiles;
             d.noop = noop;
             d.partial = partial;
+            d.x_ready = x_ready ? 1 : 0;
             if (runs_out) *runs_out = R;
             return cuda_status(ct::launch_direct(d, fmt, partial != nullptr, out_t ? 0 : 1, stream));
         }
@@ -263,6 +265,8 @@ int fp8_dbias_cast_transpose_ex(const void* dy, int64_t rows, int64_t cols, cons
                                 void* dbias, int dbias_dtype, void* workspace,
                                 size_t workspace_bytes, int fmt, const float* noop_flag,
                                 void* stream) {
+    const bool x_ready = (dbias_dtype & CT_DBIAS_X_READY) != 0;
+    dbias_dtype &= ~static_cast<int>(CT_DBIAS_X_READY);
     if (dbias_dtype != CT_DBIAS_FP32 && dbias_dtype != CT_DBIAS_BF16) return CT_ERR_ARG;
     int st = check_cast(dy, rows, cols, scale, amax, scale_inv, out, out_t, true, fmt);
     if (st != CT_OK) return st;
@@ -284,7 +288,7 @@ int fp8_dbias_cast_transpose_ex(const void* dy, int64_t rows, int64_t cols, cons
     float* partial = static_cast<float*>(workspace);
     int64_t runs = 0;
     st = cast_impl(dy, rows, cols, scale, amax, scale_inv, out, out_t, partial, fmt, noop_flag, s,
-                   &runs);
+                   &runs, x_ready);
     if (st != CT_OK) return st;
     return cuda_status(ct::launch_dbias_finish(partial, runs, cols, dbias,
                                                dbias_dtype == CT_DBIAS_BF16, noop_flag, s));

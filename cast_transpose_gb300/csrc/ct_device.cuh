@@ -199,6 +199,13 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32
                  : "memory");
 }
 
+// Bulk prefetch of `bytes` (a multiple of 16) at a 16-byte aligned global
+// address into L2: a hint with no completion signal; a later write to the
+// same lines updates them in L2, so it cannot make a read stale.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ---- 4x4 byte transpose ------------------------------------------------------
 // r0..r3 hold rows 0..3 of a 4x4 byte block (byte k = column k); on return
 // c0..c3 hold its columns (byte i = row i).

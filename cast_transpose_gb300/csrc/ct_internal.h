@@ -108,6 +108,9 @@ struct DirectParams {
     int64_t total_tiles;
     const float* noop;      // nullable device flag
     float* partial;         // dbias partials [ceil(rows/128), cols] (one row per tile row), or null
+    int x_ready;            // caller's promise: no kernel still running writes x
+                            // (the tiles may be loaded before the dependency wait)
+    int prefetch_ctas;      // CTAs (from block 0) that prefetch their tile into L2 before the wait
 };
 constexpr int64_t kDirectMinTiles = 2048;
 // `variant`: 0 = cast + transpose, 1 = cast only; `dbias` requires variant 0.

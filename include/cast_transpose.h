@@ -63,8 +63,9 @@
  *     in the stream: they may be scheduled while it still runs, and read or
  *     write nothing before it has completed.  A cast kernel may only ask for
  *     its first tiles of x to be prefetched into L2 meanwhile, a hint that
- *     cannot return stale data.  fp8_cast_transpose_ex with CT_X_READY lets
- *     it load them, under that flag's precondition.
+ *     cannot return stale data.  fp8_cast_transpose_ex with CT_X_READY (and
+ *     fp8_dbias_cast_transpose_ex with CT_DBIAS_X_READY) lets it load them,
+ *     under that flag's precondition.
  */
 #ifndef CAST_TRANSPOSE_GB300_H
 #define CAST_TRANSPOSE_GB300_H
@@ -175,11 +176,15 @@ int fp8_dbias_cast_transpose(const void* dy, int64_t rows, int64_t cols,
  * (0 when rows or cols is 0 or negative). */
 size_t fp8_dbias_cast_transpose_workspace_size(int64_t rows, int64_t cols);
 
-/* Element type of fp8_dbias_cast_transpose_ex's db output. */
+/* Element type of fp8_dbias_cast_transpose_ex's db output, optionally OR'd
+ * with CT_DBIAS_X_READY. */
 typedef enum {
     CT_DBIAS_FP32 = 0,   /* fp32, as fp8_dbias_cast_transpose                   */
-    CT_DBIAS_BF16 = 1    /* the same fp32 column sum, rounded to bf16 (nearest
+    CT_DBIAS_BF16 = 1,   /* the same fp32 column sum, rounded to bf16 (nearest
                             even; NaN -> 0x7FFF), e.g. for a bf16 bias         */
+    CT_DBIAS_X_READY = 0x100  /* the CT_X_READY promise for dy (see
+                                 ct_cast_flags): the first tiles of dy may be
+                                 loaded before the preceding kernel completes */
 } ct_dbias_dtype;
 
 /*
@@ -189,7 +194,8 @@ typedef enum {
  *
  *   dbias        [cols] output of type dbias_dtype, 4-byte (fp32) or 2-byte
  *                (bf16) aligned; must not overlap the other buffers
- *   dbias_dtype  CT_DBIAS_FP32 or CT_DBIAS_BF16
+ *   dbias_dtype  CT_DBIAS_FP32 or CT_DBIAS_BF16, optionally OR'd with
+ *                CT_DBIAS_X_READY (the caller's CT_X_READY promise for dy)
  *   (every other argument as in fp8_dbias_cast_transpose)
  *
  * Errors: as fp8_dbias_cast_transpose, plus CT_ERR_ARG for an unknown

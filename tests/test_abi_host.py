@@ -204,3 +204,14 @@ def test_fp8_convert_f32_rejects(L):
     assert f(X + 2, 100, 0, Q, None) == CT_ERR_ALIGN
     assert f(X, 100, 0, X + 399, None) == CT_ERR_ALIAS    # out starts inside the 400 input bytes
     assert f(None, 0, 0, None, None) == CT_OK              # nothing to do, nothing launched
+
+
+def test_dbias_ex_x_ready_flag(L):
+    def ex(kind, rows=300):
+        return L.fp8_dbias_cast_transpose_ex(X, rows, 70, S, A, SI, Q, QT, DB, kind, WS, 1 << 20, 1,
+                                             None, None)
+    assert ex(0x200) == CT_ERR_ARG                 # unknown flag bit
+    assert ex(0x100 | 2) == CT_ERR_ARG             # the flag does not make a bad dtype valid
+    assert ex(0x100 | 1, rows=0) == CT_OK          # empty: nothing launched
+    assert ex(0x100, rows=0) == CT_OK
+

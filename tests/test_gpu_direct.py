@@ -313,3 +313,94 @@ def test_rows_not_multiple_of_16(fmt, shape):
     q.check()
     assert np.array_equal(q.numpy().reshape(rows, cols), ref["q"])
     assert f32_bits(a.item()) == f32_bits(ref["amax"])
+
+
+def test_default_path_sees_x_written_by_the_preceding_kernel():
+    """The direct kernel's first wave asks for its tiles to be prefetched into
+    L2 before the wait for the preceding kernel (cast only and dbias, no noop
+    flag).  The kernel just before each call rewrites x (a sign flip), eagerly
+    and in a replayed graph: every call must see the new values."""
+    rows, cols = 8192, 4096                         # 2048 tiles: the direct kernel
+    x_cpu = workloads.normal_bf16(rows, cols, 1.0, 77)
+    refs = [oracle.cast_transpose(x_cpu, 1.0, ct.E4M3), oracle.cast_transpose(-x_cpu, 1.0, ct.E4M3)]
+    dbs = [oracle.dbias(x_cpu), oracle.dbias(-x_cpu)]
+    x = x_cpu.cuda()
+    qc = torch.empty(rows, cols, dtype=torch.uint8, device="cuda")
+    q, qt = ct.empty_outputs(x)
+    db = torch.empty(cols, device="cuda")
+    ws = torch.empty(ct.dbias_workspace_size(rows, cols), dtype=torch.uint8, device="cuda")
+    s, a, si = scalar(1.0), scalar(0.0), scalar(0.0)
+
+    def step():
+        x.neg_()                                    # x := -x_cpu, then the cast only
+        ct.fp8_cast(x, s, a, si, qc, ct.E4M3)
+        x.neg_()                                    # x := +x_cpu, then the dbias cast-transpose
+        ct.fp8_dbias_cast_transpose(x, s, a, si, q, qt, db, ws, ct.E4M3)
+
+    for i in range(6):
+        step()
+        torch.cuda.synchronize()
+        assert np.array_equal(qc.cpu().numpy(), refs[1]["q"]), i
+        assert np.array_equal(q.cpu().numpy(), refs[0]["q"]), i
+        assert np.array_equal(qt.cpu().numpy(), refs[0]["qt"]), i
+        assert dbias_tolerance_ok(db.cpu().numpy(), dbs[0], x_cpu), i
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side), torch.cuda.graph(g):
+        x.neg_()
+        ct.fp8_cast(x, s, a, si, qc, ct.E4M3)
+    torch.cuda.current_stream().wait_stream(side)
+    for i in range(4):                              # x flips on every replay
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(qc.cpu().numpy(), refs[(i + 1) % 2]["q"]), i
+
+
+@pytest.mark.parametrize("shape", [(8192, 4096), (4095, 4096)])
+def test_x_ready_on_the_direct_kernel(shape):
+    """CT_X_READY on the direct kernel loads the tiles before the wait for the
+    preceding kernel (here a fill of an unrelated buffer): cast-transpose and
+    dbias (CT_DBIAS_X_READY) against the oracle, eager and replayed."""
+    rows, cols = shape
+    x_cpu = workloads.gradient_matrix("cpu", rows, cols, std=1e-2, outlier_fraction=1e-3)
+    ref = oracle.cast_transpose(x_cpu, 2.0, ct.E5M2)
+    db_ref = oracle.dbias(x_cpu)
+    x = x_cpu.cuda()
+    q, qt = ct.empty_outputs(x)
+    q2, qt2 = ct.empty_outputs(x)
+    db = torch.empty(cols, device="cuda")
+    ws = torch.empty(ct.dbias_workspace_size(rows, cols), dtype=torch.uint8, device="cuda")
+    other = torch.empty(1 << 20, device="cuda")
+    s, a, si, a2, si2 = scalar(2.0), scalar(0.0), scalar(0.0), scalar(0.0), scalar(0.0)
+
+    def step():
+        other.fill_(1.0)                            # the preceding kernel does not write x
+        ct.fp8_cast_transpose(x, s, a, si, q, qt, ct.E5M2, x_ready=True)
+        ct.fp8_dbias_cast_transpose(x, s, a2, si2, q2, qt2, db, ws, ct.E5M2, x_ready=True)
+
+    def check():
+        torch.cuda.synchronize()
+        for qq, tt, aa, ii in ((q, qt, a, si), (q2, qt2, a2, si2)):
+            assert np.array_equal(qq.cpu().numpy(), ref["q"])
+            assert np.array_equal(tt.cpu().numpy(), ref["qt"])
+            assert f32_bits(aa.item()) == f32_bits(ref["amax"])
+            assert f32_bits(ii.item()) == f32_bits(ref["scale_inv"])
+        assert dbias_tolerance_ok(db.cpu().numpy(), db_ref, x_cpu)
+
+    step()
+    check()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side), torch.cuda.graph(g):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(3):
+        for t in (q, qt, q2, qt2):
+            t.zero_()
+        db.zero_()
+        a.zero_()
+        a2.zero_()
+        g.replay()
+        check()
