@@ -78,6 +78,26 @@ def _worker(conn):
                 finally:
                     sh.close()
                 conn.send(res)
+            elif kind == "encode_vs_search":
+                # the oracle's encode against the exhaustive nearest-code search
+                # over the fp32 bit patterns p0 .. p1 - 1 (< 2^31: sign clear)
+                # and the same patterns with the sign bit set (no device involved)
+                import fp8_search
+                _, p0, p1, fmt = task
+                pos = np.arange(p1 - p0, dtype=np.uint32) + np.uint32(p0)
+                ref = fp8_search.nearest_code_by_search(pos.view(np.float32), fmt)
+                res = {"bad": 0, "first_pattern": None, "got": None, "want": None}
+                for pats, want in ((pos, ref),
+                                   (pos | np.uint32(0x80000000),
+                                    np.where(ref == 0x7F, ref, ref | 0x80).astype(np.uint8))):
+                    # (the search gives 0x7F for NaN; a negative value's code is the
+                    # positive one with the sign bit, NaN stays 0x7F)
+                    mine = oracle.fp8_encode(pats.view(np.float32), fmt)
+                    nb, fb = _first_bad(mine, want)
+                    if nb and res["first_pattern"] is None:
+                        res.update(first_pattern=int(pats[fb]), got=int(mine[fb]), want=int(want[fb]))
+                    res["bad"] += nb
+                conn.send(res)
             else:
                 conn.send({"error": f"unknown task {kind!r}"})
         except Exception as e:   # reported to the parent, which raises
@@ -207,6 +227,17 @@ class OraclePool:
         bits = np.array([r["amax"] for r in res], dtype=np.float32).view(np.uint32)
         out["amax"] = np.uint32(bits.max()).view(np.float32) if len(bits) else np.float32(0)
         return out
+
+    def check_encode_against_search(self, p0, p1, fmt, chunk=1 << 18):
+        """The oracle's encode of the fp32 patterns p0 .. p1 - 1 (p1 <= 2^31,
+        the sign-clear half) and of the same patterns with the sign bit set,
+        against the exhaustive nearest-code search (tests/fp8_search.py)."""
+        assert 0 <= p0 <= p1 <= (1 << 31)
+        tasks = [("encode_vs_search", a, min(p1, a + chunk), fmt) for a in range(p0, p1, chunk)]
+        res = self._run(tasks)
+        bad = [r for r in res if r["bad"]]
+        return {"bad": sum(r["bad"] for r in res),
+                "first": (bad[0]["first_pattern"], bad[0]["got"], bad[0]["want"]) if bad else None}
 
     def check_encode_patterns(self, p0, n, fmt, chunk=None):
         """Compare the codes view (filled by the caller with the conversion of

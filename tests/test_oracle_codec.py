@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 import torch
 
+import fp8_search
 import oracle
 
 FMTS = [(oracle.E4M3, torch.float8_e4m3fn, 0x7E, 448.0),
@@ -44,27 +45,10 @@ def test_round_trip_of_every_code(oracle_lib, fmt, dtype, maxcode, maxval):
 
 
 def _brute_force_encode(p: np.ndarray, fmt: int, maxcode: int, maxval: float):
-    """Nearest FP8 value by exhaustive search over the decoded positive codes;
-    ties go to the code whose last bit is 0; beyond the largest normal the
-    result saturates.  Independent of the oracle's binade arithmetic."""
-    grid_codes = np.arange(maxcode + 1, dtype=np.int64)
-    grid = _torch_decode(torch.float8_e4m3fn if fmt == oracle.E4M3 else torch.float8_e5m2)
-    grid = grid[: maxcode + 1].astype(np.float64)
-    assert np.all(np.diff(grid) > 0)
-    with np.errstate(invalid="ignore"):      # signalling-NaN patterns among the probes
-        a = np.abs(p.astype(np.float64))
-    hi = np.clip(np.searchsorted(grid, a, side="left"), 0, maxcode)
-    lo = np.clip(hi - 1, 0, maxcode)
-    d_lo = np.abs(a - grid[lo])
-    d_hi = np.abs(grid[hi] - a)
-    pick = np.where(d_lo < d_hi, lo, hi)
-    tie = d_lo == d_hi
-    pick = np.where(tie, np.where(grid_codes[lo] % 2 == 0, lo, hi), pick)
-    pick = np.where(a >= maxval, maxcode, pick)
-    sign = np.where(np.signbit(p), 0x80, 0)
-    out = (pick | sign).astype(np.uint8)
-    out[np.isnan(p)] = 0x7F
-    return out
+    """Nearest FP8 value by exhaustive search over the decoded positive codes
+    (tests/fp8_search.py): independent of the oracle's binade arithmetic."""
+    assert maxcode == fp8_search.MAXCODE[fmt] and maxval == fp8_search.MAXVAL[fmt]
+    return fp8_search.nearest_code_by_search(p, fmt)
 
 
 def _probe_values(fmt):
