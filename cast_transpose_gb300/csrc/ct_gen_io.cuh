@@ -18,18 +18,6 @@ __device__ __forceinline__ uint32_t pick(const uint32_t (&w)[8], int j, int k) {
     return k == 0 ? a : k == 1 ? b : k == 2 ? c : d;
 }
 
-// The 8 bf16 that start at element m (0..7) of the 16 held by lo, hi.
-__device__ __forceinline__ uint4 extract8(const uint4& lo, const uint4& hi, int m) {
-    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-    const int k = m >> 1;
-    const uint32_t t0 = pick(w, 0, k), t1 = pick(w, 1, k), t2 = pick(w, 2, k),
-                   t3 = pick(w, 3, k), t4 = pick(w, 4, k);
-    if ((m & 1) == 0) return make_uint4(t0, t1, t2, t3);
-    // odd start: the high half of word k + j, then the low half of word k + j + 1
-    return make_uint4(__byte_perm(t0, t1, 0x5432), __byte_perm(t1, t2, 0x5432),
-                      __byte_perm(t2, t3, 0x5432), __byte_perm(t3, t4, 0x5432));
-}
-
 // Zero the elements n..7 of an 8-element chunk.
 __device__ __forceinline__ uint4 keep_first(uint4 v, int n) {
     uint32_t w[4] = {v.x, v.y, v.z, v.w};

@@ -37,8 +37,9 @@ namespace {
 //     registers while the copies are in flight); a chunk
 //     that crosses the end of x copies only the bytes up to it, and the one
 //     chunk that can start before x (its first) is read element by element;
-//   * pass 1: the 8 elements of chunk c come out of two staged chunks by a
-//     register shift; amax, column sums and cast as in the direct kernel;
+//   * pass 1: the 8 elements of chunk c are five aligned 4-byte words of the
+//     staged row, shifted by a uniform byte permute; amax, column sums and
+//     cast as in the direct kernel;
 //     elements past the row end are zeroed (they belong to the next row);
 //     q is stored 8 bytes per thread, as aligned words shifted across
 //     registers plus a short head and tail where the address is not aligned
@@ -47,11 +48,13 @@ namespace {
 //     and out_t is 16-byte aligned every block is one aligned 16-byte store,
 //     otherwise each column's segment of qT is written as aligned 16-byte
 //     blocks gathered from neighbouring lanes (gen::store_segment_x8).
-// Measured on GB300 (8191x12287, both dimensions odd): 3.24 TB/s, limited by
-// instruction issue (79% of scheduler cycles issue; DRAM 36% busy): the
-// shifts and partial stores that misalignment costs.  Aligned-block stores
-// for both q and qT with the end blocks written by a loop ran at 1.63 TB/s;
-// per-thread unaligned 16-byte stores of qT at 2.98 TB/s.
+// Measured on GB300 (8191x12287, both dimensions odd): 3.48 TB/s, limited by
+// instruction issue on the integer pipe (ALU 64% of peak, 79% of scheduler
+// cycles issue, DRAM 36% busy): the shifts and partial stores that
+// misalignment costs.  Measured and dropped: aligned-block stores for q and
+// qT with the end blocks written by a loop (1.63 TB/s); per-thread unaligned
+// 16-byte stores of qT (2.98); q and qT written as aligned blocks from
+// shared-memory words in a phase of their own after pass 1 (2.80).
 constexpr int kStageRow = 17 * 16;   // staged bytes per tile row
 constexpr int kGenSmem = kTileRows * kStageRow + kTileRows * kTileCols;
 constexpr int kGenSmemDbias = kGenSmem + 8 * dev::kColsumStride * 4;
@@ -124,22 +127,25 @@ __global__ void __launch_bounds__(256, DBIAS ? 3 : 4) general_cast_kernel(Genera
 #pragma unroll
         for (int j = 0; j < 8; ++j) cs[j] = 0.0f;
         const int nv = ncol - 8 * c <= 0 ? 0 : (ncol - 8 * c >= 8 ? 8 : ncol - 8 * c);
-        // byte offset in x of this thread's first row segment, and its step
-        uint32_t xoff = static_cast<uint32_t>(
-            (xbeg + 2 * uintptr_t((row0 + rg) * cols + col0)) & 15);
-        const uint32_t xstep = static_cast<uint32_t>((32 * uintptr_t(cols)) & 15);
+        // Byte offset (even) of this thread's row segments within their first
+        // staged chunk: the same for rows rg + 16*it (16 rows of x are a
+        // multiple of 16 bytes).  Its 8 elements are words wo .. wo+4 of the
+        // staged chunks, shifted by 2 bytes when mx % 4 == 2: five aligned
+        // 4-byte shared loads and four byte permutes with a uniform selector.
+        const int mx = static_cast<int>((xbeg + 2 * uintptr_t((row0 + rg) * cols + col0)) & 15);
+        const int wo = mx >> 2;
+        const uint32_t sel = (mx & 2) ? 0x5432u : 0x3210u;
 #pragma unroll 2
         for (int it = 0; it < 8; ++it) {
             const int r = rg + 16 * it;
             const int64_t row = row0 + r;
             const int n = r < nrow ? nv : 0;
-            const int mx = static_cast<int>(xoff);
-            xoff = (xoff + xstep) & 15;
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
             if (n > 0) {
-                const uint8_t* rp = xs + r * kStageRow + 16 * c;
-                v = *reinterpret_cast<const uint4*>(rp);
-                if (mx != 0) v = gen::extract8(v, *reinterpret_cast<const uint4*>(rp + 16), mx >> 1);
+                const uint32_t* rp = reinterpret_cast<const uint32_t*>(xs + r * kStageRow + 16 * c) + wo;
+                const uint32_t w0 = rp[0], w1 = rp[1], w2 = rp[2], w3 = rp[3], w4 = rp[4];
+                v = make_uint4(__byte_perm(w0, w1, sel), __byte_perm(w1, w2, sel),
+                               __byte_perm(w2, w3, sel), __byte_perm(w3, w4, sel));
                 if (n < 8) v = gen::keep_first(v, n);
             }
             amax_pair = dev::absmax_pair(amax_pair, v.x);
