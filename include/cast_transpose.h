@@ -51,10 +51,10 @@
  *     CT_ERR_CUDA.  Any shape and alignment is accepted.  Shapes with rows
  *     a multiple of 16 and cols a multiple of 8, with 16-byte-aligned
  *     buffers, take a fast path: a persistent TMA-staged kernel for launches
- *     under 2048 tiles of 128x128, a one-tile-per-CTA direct-load kernel from
- *     2048 tiles on.  Other row counts with cols a multiple of 8 and aligned
- *     buffers take the direct-load kernel.  Everything else takes a slower
- *     general kernel.  All give identical results.
+ *     under 2048 tiles of 128x128, a direct-load kernel (256 threads per
+ *     tile) from 2048 tiles on.  Other row counts with cols a multiple of 8
+ *     and aligned buffers take the direct-load kernel.  Everything else takes
+ *     a slower general kernel.  All give identical results.
  *   - Calls are thread-safe; the library keeps no per-call state.  The first
  *     call of an entry point on a device also sets its kernels' shared-memory
  *     limit (cudaFuncSetAttribute, once per device): make that first call
