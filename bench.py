@@ -30,7 +30,7 @@ sample of the same workload.
 Secondary lines (under "secondary", each with its own rate): the weight-like
 4096x4096 step (8 casts + 8 updates, with and without CT_X_READY), the
 gradient-like 8192x12288 dbias cast-transpose (E5M2), the activation
-16384x12288 cast-transpose with the noop flag clear and set, the 256x512
+16384x12288 cast-transpose without a noop flag and with one clear and set, the 256x512
 matrix, cast only, the FP8 transpose and a ragged 8191x12287 matrix.
 """
 from __future__ import annotations
@@ -680,15 +680,20 @@ def secondary(dev, peaks, args) -> dict:
         "direct_cast_transpose_kernel (dbias) + dbias_finish_kernel; the first tiles of dy are "
         "loaded while the previous call's finish kernel runs (nothing writes dy)")
     del dy, q, qt, db, ws
-    # activation 16384x12288: cast-transpose, the launch with the noop flag set,
-    # cast only, FP8 transpose
+    # activation 16384x12288: cast-transpose without and with a noop flag (clear,
+    # then set), cast only, FP8 transpose
     x = workloads.activation_matrix(dev)
     q, qt = ct.empty_outputs(x)
+    ms, best = _timed(torch, lambda: ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3))
+    res["cast_transpose 16384x12288 E4M3"] = _rate_entry(
+        ms, best, 4 * x.numel() + 12, peaks, "direct_cast_transpose_kernel")
     flag = torch.zeros(1, device=dev)
     ms, best = _timed(torch, lambda: ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3,
                                                            noop_flag=flag))
     res["cast_transpose 16384x12288 E4M3, noop flag 0"] = _rate_entry(
-        ms, best, 4 * x.numel() + 12, peaks, "direct_cast_transpose_kernel")
+        ms, best, 4 * x.numel() + 12, peaks,
+        "direct_loop_kernel: a looping first wave over 80% of the tiles, then one tile per "
+        "256 threads")
     ms, best = _timed(torch, lambda: ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3,
                                                            x_ready=True))
     res["cast_transpose 16384x12288 E4M3, CT_X_READY"] = _rate_entry(
@@ -700,8 +705,9 @@ def secondary(dev, peaks, args) -> dict:
                                                            noop_flag=flag), per_graph=50)
     res["cast_transpose 16384x12288 E4M3, noop flag 1"] = {
         "us": round(ms * 1e3, 2), "us_best": round(best * 1e3, 2),
-        "note": "the same launch skipped by the flag: every CTA starts, waits for the preceding "
-                "kernel, reads the flag and exits"}
+        "note": "the same launch skipped by the flag: each of its CTAs (the looping first wave "
+                "and the 1280 after it) starts, waits for the preceding kernel, reads the flag "
+                "and exits"}
     ms, best = _timed(torch, lambda: ct.fp8_cast(x, s1, a0, si0, q, ct.E4M3))
     res["cast 16384x12288 E4M3"] = _rate_entry(ms, best, 3 * x.numel() + 12, peaks,
                                                "direct_cast_transpose_kernel (cast only)")
@@ -961,6 +967,8 @@ def profile_case(name: str) -> None:
       'cast':       cast only of the activation, then three FP8 transposes;
       'general':    cast-transpose of a ragged 8191x12287 matrix, then three
                     FP8 transposes of its q (the general kernels);
+      'loop':       the same with a noop flag at 0 (the looping grid that calls
+                    with a noop flag take);
       'noop':       three launches of the activation cast-transpose with the
                     noop flag set;
       'weight':     three steps of the weight-like 4096x4096 workload (eight
@@ -1003,10 +1011,11 @@ def profile_case(name: str) -> None:
             ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3)
         for _ in range(3):
             ct.fp8_transpose(q, qt)
-    elif name in ("activation", "noop"):
+    elif name in ("activation", "loop", "noop"):
         x = workloads.activation_matrix(dev)
         q, qt = ct.empty_outputs(x)
-        flag = torch.full((1,), 1.0 if name == "noop" else 0.0, device=dev)
+        flag = None if name == "activation" else \
+            torch.full((1,), 1.0 if name == "noop" else 0.0, device=dev)
         for _ in range(3):
             ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3, noop_flag=flag)
     elif name == "weight":
@@ -1045,8 +1054,8 @@ def _parse(argv=None):
     ap.add_argument("--extra", action=argparse.BooleanOptionalAction, default=True,
                     help="also time the secondary workloads")
     ap.add_argument("--profile-case",
-                    choices=["activation", "gradient", "list", "cast", "general", "noop",
-                             "weight"],
+                    choices=["activation", "gradient", "list", "cast", "general", "loop",
+                             "noop", "weight"],
                     default=None,
                     help="only run 3 launches of one workload's kernel (for ncu) and exit")
     return ap.parse_args(argv)

@@ -23,6 +23,11 @@
 // one tile's loads is hidden by the other resident tiles.  Grids cover the
 // tile count (thousands of CTAs, many waves of 152 SMs x 4 tiles); the TMA
 // kernel keeps the launches too small for that to pay.
+//
+// Calls that pass a noop flag take direct_loop_kernel instead: the same
+// passes, but a first wave of CTAs that loops over most of the tiles, so a
+// launch that its flag skips starts a few waves of CTAs instead of
+// thousands.
 #include "ct_device.cuh"
 #include "ct_gen_io.cuh"
 #include "ct_internal.h"
@@ -48,6 +53,8 @@ constexpr int kDirectWarps = kDirectThreads / 32;
 
 template <bool WRITE_T, bool DBIAS>
 constexpr int tiles_per_cta() { return WRITE_T && !DBIAS ? 2 : 1; }
+
+constexpr int64_t kLoopPercent = 80;
 
 // The tensor of a list launch that owns global tile `tile`: the last entry
 // whose first tile is <= tile (entries are non-empty and in tile order).
@@ -246,6 +253,143 @@ __global__ void __launch_bounds__(kDirectThreads * TPC, 4 / TPC)
     }
 }
 
+
+// First row and column of tile `tile` of a tensor with `tc` tiles per row.
+__device__ __forceinline__ int2 loop_tile(int tile, int tc) {
+    const int rt = tile / tc;
+    return make_int2(rt * kTileRows, (tile - rt * tc) * kTileCols);
+}
+
+// The eight 16-byte loads of one thread (rows rg + 16 * it of column chunk c)
+// of the tile at (row0, col0); rows % 16 == 0, rows and cols below 2^31.
+__device__ __forceinline__ void loop_load(const uint16_t* x, int rows, int cols, int2 t, int c,
+                                          int rg, uint4 (&v)[8]) {
+    const bool col_ok = t.y + 8 * c < cols;
+    const int nr = (rows - t.x) >> 4;   // 16-row blocks left in the tensor
+    const uint16_t* src = x + static_cast<int64_t>(t.x + rg) * cols + t.y + 8 * c;
+#pragma unroll
+    for (int it = 0; it < 8; ++it)
+        v[it] = (col_ok && it < nr)
+                    ? __ldcs(reinterpret_cast<const uint4*>(src + static_cast<int64_t>(16 * it) * cols))
+                    : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Cast + transpose of one tensor (rows % 16 == 0) for calls that pass a
+// noop flag.  Every CTA of the direct kernel starts, waits, reads the flag
+// and exits, so a skipped launch costs about one CTA turnover per tile pair
+// (6.8 us at 16384x12288).  Here the first wave of CTAs (loop_ctas: SMs x 2)
+// loops: group gi of its G = 2 * loop_ctas groups takes tiles gi + k * G for
+// k < loop_tiles, loading tile k + 1 into registers as soon as pass 2 has
+// read tile k out of the shared copy, i.e. during its qT stores.  The CTAs
+// after the first wave take one tile per group from the remainder, as the
+// direct kernel does; the hardware hands them to whichever SM frees a slot
+// first, which evens out SMs that stream slower than others (measured per
+// group on GB300: 5.0 to 6.4 us per tile, so a grid that only loops ends
+// with its slowest SM, 140 against 117 us).
+template <int FMT, int TPC>
+__global__ void __launch_bounds__(kDirectThreads * TPC, 4 / TPC)
+    direct_loop_kernel(const __grid_constant__ DirectParams<1> p) {
+    dev::pdl_launch_dependents();
+    dev::pdl_wait();
+    if (p.noop != nullptr && *p.noop != 0.0f) return;
+
+    __shared__ __align__(16) uint8_t sq_all[TPC][kTileRows * kTileCols];
+    __shared__ unsigned s_amax_all[TPC][kDirectWarps];
+    const int g = TPC == 1 ? 0 : static_cast<int>(threadIdx.x / kDirectThreads);
+    const int tid = threadIdx.x % kDirectThreads, lane = tid & 31, warp = tid >> 5;
+    const int total = static_cast<int>(p.total_tiles);
+    // CTAs below loop_ctas: group gi takes tiles gi + k * stride, k < loop_tiles;
+    // the CTAs after them take one tile per group from the remainder.
+    const int stride = p.loop_ctas * TPC;
+    int tile, last;
+    if (static_cast<int>(blockIdx.x) < p.loop_ctas) {
+        tile = static_cast<int>(blockIdx.x) * TPC + g;
+        last = tile + (p.loop_tiles - 1) * stride;
+    } else {
+        tile = stride * p.loop_tiles + (static_cast<int>(blockIdx.x) - p.loop_ctas) * TPC + g;
+        last = tile;
+    }
+    if (last >= total) last = total - 1;
+    if (tile >= total) return;   // a whole group: no barrier involves it
+    uint8_t* sq = sq_all[g];
+    const FastTensor& T = p.t[0];
+    const int rows = static_cast<int>(T.rows), cols = static_cast<int>(T.cols);
+    const int tc = static_cast<int>(T.tile_cols);
+    const float scale = *T.scale;
+    const int c = tid & 15, rg = tid >> 4;
+    const int b = lane & 7, w = warp * 4 + (lane >> 3);   // pass-2 mapping
+
+    uint4 v[8];
+    loop_load(p.x[0], rows, cols, loop_tile(tile, tc), c, rg, v);
+    uint32_t amax_pair = 0;
+    for (;;) {
+        int2 t = loop_tile(tile, tc);
+        {
+            const bool col_ok = t.y + 8 * c < cols;
+            const int nr = (rows - t.x) >> 4;
+            uint8_t* qrow = T.out + static_cast<int64_t>(t.x + rg) * cols + t.y + 8 * c;
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int r = rg + 16 * it;
+                amax_pair = dev::absmax_pair(amax_pair, v[it].x);
+                amax_pair = dev::absmax_pair(amax_pair, v[it].y);
+                amax_pair = dev::absmax_pair(amax_pair, v[it].z);
+                amax_pair = dev::absmax_pair(amax_pair, v[it].w);
+                const uint2 q8 = dev::cast8<FMT>(v[it], scale);
+                if (col_ok && it < nr)
+                    __stcs(reinterpret_cast<uint2*>(qrow + static_cast<int64_t>(16 * it) * cols), q8);
+                *reinterpret_cast<uint2*>(sq + r * kTileCols + ((2 * c) ^ dev::swz(r)) * 4) = q8;
+            }
+        }
+        tile_sync<TPC>(g);
+        if (tile == 0 && tid == 0) *T.scale_inv = __fdiv_rn(1.0f, scale);
+
+        uint32_t o[4][4];
+        {
+            const uint32_t* sq32 = reinterpret_cast<const uint32_t*>(sq);
+            uint32_t rw[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int r = 16 * b + j;
+                rw[j] = sq32[r * (kTileCols / 4) + (w ^ dev::swz(r))];
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                dev::transpose4x4(rw[4 * k], rw[4 * k + 1], rw[4 * k + 2], rw[4 * k + 3], o[0][k],
+                                  o[1][k], o[2][k], o[3][k]);
+        }
+        // qT columns 0-1 of the block, the next tile's loads, columns 2-3
+        const bool row_ok = t.x + 16 * b < rows;
+        uint8_t* dst = T.out_t + static_cast<int64_t>(t.y + 4 * w) * rows + t.x + 16 * b;
+        const int next = tile + stride;
+#pragma unroll
+        for (int kq = 0; kq < 2; ++kq)
+            if (row_ok && t.y + 4 * w + kq < cols)
+                __stcs(reinterpret_cast<uint4*>(dst + static_cast<int64_t>(kq) * rows),
+                       make_uint4(o[kq][0], o[kq][1], o[kq][2], o[kq][3]));
+        if (next <= last) loop_load(p.x[0], rows, cols, loop_tile(next, tc), c, rg, v);
+#pragma unroll
+        for (int kq = 2; kq < 4; ++kq)
+            if (row_ok && t.y + 4 * w + kq < cols)
+                __stcs(reinterpret_cast<uint4*>(dst + static_cast<int64_t>(kq) * rows),
+                       make_uint4(o[kq][0], o[kq][1], o[kq][2], o[kq][3]));
+        if (next > last) break;
+        tile = next;
+        tile_sync<TPC>(g);   // every thread has read the copy before it is rewritten
+    }
+
+    unsigned* s_amax = s_amax_all[g];
+    const unsigned m = __reduce_max_sync(0xFFFFFFFFu, dev::pair_to_f32_bits(amax_pair));
+    if (lane == 0) s_amax[warp] = m;
+    tile_sync<TPC>(g);
+    if (tid == 0) {
+        unsigned a = s_amax[0];
+#pragma unroll
+        for (int k = 1; k < kDirectWarps; ++k) a = a > s_amax[k] ? a : s_amax[k];
+        if (a != 0) atomicMax(reinterpret_cast<unsigned*>(T.amax), a);
+    }
+}
+
 // SMs of the current device (cached per device).
 int sm_count() {
     static std::mutex mu;
@@ -290,6 +434,25 @@ cudaError_t launch_one(const DirectParams<NT>& p, cudaStream_t stream) {
     // 8191x12288)
     if constexpr (NT == 1 && TPC != 1)
         if (p.t[0].rows % 16 != 0) return launch_tpc<NT, FMT, WRITE_T, DBIAS, 1>(p, stream);
+    // Calls with a noop flag: the looping first wave covers kLoopPercent of
+    // the tiles.  Measured at 16384x12288 on GB300, flag 0 / flag 1:
+    // 60% 6.81 TB/s / 3.4 us, 70% 6.78 / 2.9, 80% 6.75 / 2.25, 90% 6.60 / 1.6;
+    // the direct kernel 6.90 TB/s / 6.8 us.
+    if constexpr (NT == 1 && TPC == 2 && FMT >= 0) {
+        const int sms = sm_count();
+        if (p.noop != nullptr && !p.x_ready && sms > 0 && p.t[0].rows < INT_MAX &&
+            p.t[0].cols < INT_MAX && p.total_tiles < INT_MAX / 2) {
+            DirectParams<1> q = p;
+            q.loop_ctas = sms * (4 / TPC);
+            const int64_t groups = static_cast<int64_t>(q.loop_ctas) * TPC;
+            q.loop_tiles = static_cast<int>(p.total_tiles * kLoopPercent / 100 / groups);
+            if (q.loop_tiles < 1) q.loop_tiles = 1;
+            const int64_t rest = p.total_tiles - groups * q.loop_tiles;
+            const int64_t grid = q.loop_ctas + (rest > 0 ? (rest + TPC - 1) / TPC : 0);
+            const dim3 g(static_cast<unsigned>(grid)), b(kDirectThreads * TPC);
+            return launch_pdl(direct_loop_kernel<FMT, TPC>, g, b, 0, stream, q);
+        }
+    }
     return launch_tpc<NT, FMT, WRITE_T, DBIAS, TPC>(p, stream);
 }
 

@@ -41,6 +41,18 @@ def test_ragged_cast_transpose(fmt, shape):
     assert_same_cast(got, oracle.cast_transpose(x_cpu, 2.5, fmt, amax_in=0.125))
 
 
+@pytest.mark.parametrize("fmt", [ct.E4M3, ct.E5M2])
+@pytest.mark.parametrize("shape", RAGGED + [(8192, 8200)])
+def test_noop_flag_zero(fmt, shape):
+    """A call given a noop flag (here 0) takes the looping grid of a few
+    waves: ragged tile counts (an odd count leaves a CTA half idle) and, at
+    8192 x 8200, about 7 tiles per group of 256 threads."""
+    rows, cols = shape
+    x_cpu = workloads.normal_bf16(rows, cols, 50.0, 700 + rows + cols)
+    got = cast_transpose_gpu(x_cpu.cuda(), 0.375, fmt, amax_in=0.25, noop=scalar(0.0))
+    assert_same_cast(got, oracle.cast_transpose(x_cpu, 0.375, fmt, amax_in=0.25))
+
+
 def test_all_bf16_patterns_tiled():
     """Every bf16 pattern, repeated to a 4096 x 8192 matrix (2048 tiles)."""
     base = workloads.bf16_all_patterns().reshape(-1)
