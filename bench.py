@@ -31,7 +31,8 @@ Secondary lines (under "secondary", each with its own rate): the weight-like
 4096x4096 step (8 casts + 8 updates, with and without CT_X_READY), the
 gradient-like 8192x12288 dbias cast-transpose (E5M2), the activation
 16384x12288 cast-transpose without a noop flag and with one clear and set, the 256x512
-matrix, cast only, the FP8 transpose and a ragged 8191x12287 matrix.
+matrix, cast only, the FP8 transpose and a ragged 8191x12287 matrix (cast-transpose
+and cast only).
 """
 from __future__ import annotations
 
@@ -721,6 +722,9 @@ def secondary(dev, peaks, args) -> dict:
     ms, best = _timed(torch, lambda: ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3))
     res["cast_transpose 8191x12287 E4M3 (ragged)"] = _rate_entry(ms, best, 4 * x.numel() + 12,
                                                                  peaks, "general_cast_kernel")
+    ms, best = _timed(torch, lambda: ct.fp8_cast(x, s1, a0, si0, q, ct.E4M3))
+    res["cast 8191x12287 E4M3 (ragged)"] = _rate_entry(ms, best, 3 * x.numel() + 12, peaks,
+                                                       "cast_flat_kernel")
     del x, q, qt
     # the small 256x512 matrix (launch-bound: microseconds)
     x = workloads.single_matrix(dev)

@@ -179,6 +179,16 @@ int cast_impl(const void* x, int64_t rows, int64_t cols, const float* scale, flo
         if (runs_out) *runs_out = ct::dbias_units(R, R < ct::kDbiasBand ? R : ct::kDbiasBand).bands;
         return cuda_status(ct::launch_fast(p, fmt, partial != nullptr, out_t ? 0 : 1, stream));
     }
+    // A plain cast with x 16-byte and q 8-byte aligned: one flat array of
+    // rows * cols elements, whatever the row length.  (With a transpose, the
+    // flat cast followed by the FP8 transpose of q measured 2% faster than
+    // the general kernel on 8191x12287 and 9% slower with cols % 8 == 4, so
+    // cast-transpose stays on the general kernel.)
+    if (out_t == nullptr && partial == nullptr && out != nullptr && aligned(x, 16) &&
+        aligned(out, 8))
+        return cuda_status(ct::launch_cast_flat(static_cast<const uint16_t*>(x), rows * cols,
+                                                static_cast<uint8_t*>(out), scale, amax, scale_inv,
+                                                fmt, noop, stream));
     ct::GeneralArgs a;
     a.x = static_cast<const uint16_t*>(x);
     a.out = static_cast<uint8_t*>(out);

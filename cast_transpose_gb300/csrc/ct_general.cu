@@ -469,6 +469,77 @@ __global__ void __launch_bounds__(256) transpose_general_kernel(const uint8_t* _
 }
 
 // ---------------------------------------------------------------------------
+// Flat cast: q[i] = fp8(x[i] * scale) over the n = rows * cols elements as
+// one array.  The cast of an element does not depend on where its row
+// starts, so with x 16-byte and q 8-byte aligned every 8-element chunk is one
+// 16-byte load and one 8-byte store for any row length.  A CTA takes
+// kFlatChunks consecutive chunks (its threads' eight loads all in flight, as
+// in the direct kernel), and grids of thousands of CTAs let the hardware
+// balance the SMs.  The n % 8 elements after the last whole chunk are
+// converted by one thread.  Amax and scale_inv as in the tile kernels.
+constexpr int kFlatPerThread = 8;
+constexpr int64_t kFlatChunks = 256 * kFlatPerThread;
+
+template <int FMT>
+__global__ void __launch_bounds__(256) cast_flat_kernel(const uint16_t* __restrict__ x, int64_t n,
+                                                        uint8_t* __restrict__ q, const float* scale_p,
+                                                        float* amax, float* scale_inv,
+                                                        const float* noop) {
+    dev::pdl_launch_dependents();
+    dev::pdl_wait();
+    if (noop != nullptr && *noop != 0.0f) return;
+    __shared__ unsigned s_amax[8];
+    const float scale = *scale_p;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t chunks = n >> 3;
+    const int64_t c0 = int64_t(blockIdx.x) * kFlatChunks + tid;
+    uint4 v[kFlatPerThread];
+#pragma unroll
+    for (int u = 0; u < kFlatPerThread; ++u) {
+        const int64_t ch = c0 + 256 * u;
+        v[u] = ch < chunks ? __ldcs(reinterpret_cast<const uint4*>(x) + ch) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    uint32_t amax_pair = 0;
+#pragma unroll
+    for (int u = 0; u < kFlatPerThread; ++u) {
+        const int64_t ch = c0 + 256 * u;
+        amax_pair = dev::absmax_pair(amax_pair, v[u].x);
+        amax_pair = dev::absmax_pair(amax_pair, v[u].y);
+        amax_pair = dev::absmax_pair(amax_pair, v[u].z);
+        amax_pair = dev::absmax_pair(amax_pair, v[u].w);
+        if (ch < chunks) reinterpret_cast<uint2*>(q)[ch] = dev::cast8<FMT>(v[u], scale);
+    }
+    if (blockIdx.x == 0 && tid == 0) {
+        const int64_t t0 = chunks << 3;
+        if (t0 < n) {   // the last n % 8 elements
+            uint32_t e[4] = {0u, 0u, 0u, 0u};
+            for (int64_t i = t0; i < n; ++i)
+                e[(i - t0) >> 1] |= uint32_t(x[i]) << (16 * ((i - t0) & 1));
+            const uint4 t = make_uint4(e[0], e[1], e[2], e[3]);
+            amax_pair = dev::absmax_pair(amax_pair, t.x);
+            amax_pair = dev::absmax_pair(amax_pair, t.y);
+            amax_pair = dev::absmax_pair(amax_pair, t.z);
+            amax_pair = dev::absmax_pair(amax_pair, t.w);
+            const uint2 c = dev::cast8<FMT>(t, scale);
+            for (int64_t i = t0; i < n; ++i) {
+                const int k = static_cast<int>(i - t0);
+                q[i] = static_cast<uint8_t>((k < 4 ? c.x : c.y) >> (8 * (k & 3)));
+            }
+        }
+        *scale_inv = __fdiv_rn(1.0f, scale);
+    }
+    const unsigned m = __reduce_max_sync(0xFFFFFFFFu, dev::pair_to_f32_bits(amax_pair));
+    if (lane == 0) s_amax[warp] = m;
+    __syncthreads();
+    if (tid == 0) {
+        unsigned a = s_amax[0];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) a = a > s_amax[w] ? a : s_amax[w];
+        if (a != 0) atomicMax(reinterpret_cast<unsigned*>(amax), a);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // The conversion step alone: out[i] = fp8(in[i]) through dev::cvt_fp8x2, the
 // routine every cast kernel applies to x * scale.  Grid-stride over pairs of
 // values; a trailing odd value is converted with a zero partner whose code is
@@ -567,6 +638,18 @@ cudaError_t launch_convert_f32(const float* in, int64_t n, int fmt, uint8_t* out
     const dim3 grid(grid_for(((n + 1) / 2 + 255) / 256, 152 * 16)), block(256);
     return fmt == 0 ? launch_pdl(convert_f32_kernel<0>, grid, block, 0, stream, in, n, out)
                     : launch_pdl(convert_f32_kernel<1>, grid, block, 0, stream, in, n, out);
+}
+
+cudaError_t launch_cast_flat(const uint16_t* x, int64_t n, uint8_t* q, const float* scale,
+                             float* amax, float* scale_inv, int fmt, const float* noop,
+                             cudaStream_t stream) {
+    const int64_t chunks = n >> 3;
+    const dim3 grid(grid_for((chunks + kFlatChunks - 1) / kFlatChunks, int64_t(1) << 30)), block(256);
+    if (fmt == 0)
+        return launch_pdl(cast_flat_kernel<0>, grid, block, 0, stream, x, n, q, scale, amax,
+                          scale_inv, noop);
+    return launch_pdl(cast_flat_kernel<1>, grid, block, 0, stream, x, n, q, scale, amax, scale_inv,
+                      noop);
 }
 
 cudaError_t launch_transpose(const uint8_t* in, int64_t rows, int64_t cols, uint8_t* out,
