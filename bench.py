@@ -971,6 +971,8 @@ def profile_case(name: str) -> None:
       'cast':       cast only of the activation, then three FP8 transposes;
       'general':    cast-transpose of a ragged 8191x12287 matrix, then three
                     FP8 transposes of its q (the general kernels);
+      'flat':       three plain casts of the ragged 8191x12287 matrix (the flat
+                    cast kernel);
       'loop':       the same with a noop flag at 0 (the looping grid that calls
                     with a noop flag take);
       'noop':       three launches of the activation cast-transpose with the
@@ -1015,6 +1017,11 @@ def profile_case(name: str) -> None:
             ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3)
         for _ in range(3):
             ct.fp8_transpose(q, qt)
+    elif name == "flat":
+        x = workloads.normal_bf16(8191, 12287, 1.0, 17, dev)
+        q, qt = ct.empty_outputs(x)
+        for _ in range(3):
+            ct.fp8_cast(x, s1, a0, si0, q, ct.E4M3)
     elif name in ("activation", "loop", "noop"):
         x = workloads.activation_matrix(dev)
         q, qt = ct.empty_outputs(x)
@@ -1058,8 +1065,8 @@ def _parse(argv=None):
     ap.add_argument("--extra", action=argparse.BooleanOptionalAction, default=True,
                     help="also time the secondary workloads")
     ap.add_argument("--profile-case",
-                    choices=["activation", "gradient", "list", "cast", "general", "loop",
-                             "noop", "weight"],
+                    choices=["activation", "gradient", "list", "cast", "general", "flat",
+                             "loop", "noop", "weight"],
                     default=None,
                     help="only run 3 launches of one workload's kernel (for ncu) and exit")
     return ap.parse_args(argv)
