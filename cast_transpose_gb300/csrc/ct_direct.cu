@@ -56,6 +56,7 @@ constexpr int tiles_per_cta() { return WRITE_T && !DBIAS ? 2 : 1; }
 
 constexpr int64_t kLoopPercent = 80;
 
+
 // The tensor of a list launch that owns global tile `tile`: the last entry
 // whose first tile is <= tile (entries are non-empty and in tile order).
 template <int NT>
@@ -132,8 +133,9 @@ __global__ void __launch_bounds__(kDirectThreads * TPC, 4 / TPC)
     // the caller's promise that no running kernel writes x (x_ready), the
     // tile itself is loaded; otherwise the CTAs of the first wave -- the ones
     // that can be resident while the preceding kernel still runs -- only ask
-    // for their tile rows to be prefetched into L2, a hint that cannot return
-    // stale data (every write lands in L2).
+    // for their tile rows, and those of the second wave's tiles, to be
+    // prefetched into L2: a hint that cannot return stale data (every write
+    // lands in L2).
     bool loaded = false;
     if constexpr (EARLY) {
         if (early) {
@@ -146,10 +148,20 @@ __global__ void __launch_bounds__(kDirectThreads * TPC, 4 / TPC)
                                 : make_uint4(0u, 0u, 0u, 0u);
                 }
                 loaded = true;
-            } else if (tid < kTileRows && row0 + tid < rows) {
-                const int64_t ncols = cols - col0 < kTileCols ? cols - col0 : kTileCols;
-                dev::prefetch_l2_bulk(p.x[ti] + (row0 + tid) * cols + col0,
-                                      static_cast<uint32_t>(2 * ncols));
+            } else if constexpr (NT == 1) {
+                // threads 0..127: row tid of this CTA's tile; threads 128..255:
+                // row tid - 128 of the tile of the CTA one wave later (whose
+                // own first loads then find its rows in L2)
+                const int64_t tp = tile + (tid < kTileRows ? 0 : int64_t(p.prefetch_ctas) * TPC);
+                if (tp < p.total_tiles) {
+                    const int64_t rtp = tp / T.tile_cols;
+                    const int64_t rp = rtp * kTileRows + (tid & (kTileRows - 1));
+                    const int64_t cp = (tp - rtp * T.tile_cols) * kTileCols;
+                    if (rp < rows) {
+                        const int64_t ncp = cols - cp < kTileCols ? cols - cp : kTileCols;
+                        dev::prefetch_l2_bulk(p.x[ti] + rp * cols + cp, static_cast<uint32_t>(2 * ncp));
+                    }
+                }
             }
             dev::pdl_wait();
             if (p.noop != nullptr && *p.noop != 0.0f) return;
@@ -408,11 +420,14 @@ int sm_count() {
 template <int NT, int FMT, bool WRITE_T, bool DBIAS, int TPC>
 cudaError_t launch_tpc(const DirectParams<NT>& p, cudaStream_t stream) {
     const int64_t grid = (p.total_tiles + TPC - 1) / TPC;
-    // The first wave (SMs x resident CTAs) prefetches its tiles into L2 before
-    // the dependency wait, on the one-tile-per-CTA variants of calls that
-    // have no noop flag.  Measured on GB300: dbias 8192x12288 65.1 -> 63.3 us,
-    // cast only +1.7%; with two tiles per CTA the prefetch cost 2.5-3%, and a
-    // call that its flag skips would still pay for the prefetch (6.8 -> 12.4 us).
+    // The first wave (SMs x resident CTAs) prefetches its tiles, and the
+    // second wave's, into L2 before the dependency wait, on the
+    // one-tile-per-CTA variants of calls that have no noop flag.  Measured on
+    // GB300: dbias 8192x12288 65.1 -> 63.3 us with the first wave's tiles,
+    // 62.6 -> 61.6 us adding the second's (a third and fourth: 62.5, 63.5 us);
+    // cast only +1.7%, then +0.5%.  With two tiles per CTA the prefetch cost
+    // 2.5-3%, and a call that its flag skips would still pay for the prefetch
+    // (6.8 -> 12.4 us).
     const dim3 g(static_cast<unsigned>(grid)), b(kDirectThreads * TPC);
     if constexpr (NT == 1) {   // lists never work early
         DirectParams<1> q = p;
