@@ -148,6 +148,22 @@ __global__ void __launch_bounds__(kDirectThreads * TPC, 4 / TPC)
                                 : make_uint4(0u, 0u, 0u, 0u);
                 }
                 loaded = true;
+                // and the first wave's CTAs ask for the second wave's tiles, as below
+                if constexpr (NT == 1) {
+                    if (blockIdx.x < p.prefetch_ctas && tid < kTileRows) {
+                        const int64_t tp = tile + int64_t(p.prefetch_ctas) * TPC;
+                        if (tp < p.total_tiles) {
+                            const int64_t rtp = tp / T.tile_cols;
+                            const int64_t rp = rtp * kTileRows + tid;
+                            const int64_t cp = (tp - rtp * T.tile_cols) * kTileCols;
+                            if (rp < rows) {
+                                const int64_t ncp = cols - cp < kTileCols ? cols - cp : kTileCols;
+                                dev::prefetch_l2_bulk(p.x[ti] + rp * cols + cp,
+                                                      static_cast<uint32_t>(2 * ncp));
+                            }
+                        }
+                    }
+                }
             } else if constexpr (NT == 1) {
                 // threads 0..127: row tid of this CTA's tile; threads 128..255:
                 // row tid - 128 of the tile of the CTA one wave later (whose
