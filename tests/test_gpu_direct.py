@@ -327,12 +327,16 @@ def test_rows_not_multiple_of_16(fmt, shape):
     assert f32_bits(a.item()) == f32_bits(ref["amax"])
 
 
-def test_default_path_sees_x_written_by_the_preceding_kernel():
-    """The direct kernel's first wave asks for its tiles to be prefetched into
-    L2 before the wait for the preceding kernel (cast only and dbias, no noop
-    flag).  The kernel just before each call rewrites x (a sign flip), eagerly
-    and in a replayed graph: every call must see the new values."""
-    rows, cols = 8192, 4096                         # 2048 tiles: the direct kernel
+@pytest.mark.parametrize("rows", [8192, 4096])
+def test_default_path_sees_x_written_by_the_preceding_kernel(rows):
+    """The direct kernel's first wave asks for its tiles, and the second
+    wave's, to be prefetched into L2 before the wait for the preceding kernel
+    (cast only and dbias, no noop flag); the persistent TMA kernel asks for
+    all of its tiles.  The kernel just before each call rewrites x (a sign
+    flip), eagerly and in a replayed graph: every call must see the new
+    values.  8192 x 4096 is 2048 tiles (the direct kernel), 4096 x 4096 is
+    1024 (the TMA kernel)."""
+    cols = 4096
     x_cpu = workloads.normal_bf16(rows, cols, 1.0, 77)
     refs = [oracle.cast_transpose(x_cpu, 1.0, ct.E4M3), oracle.cast_transpose(-x_cpu, 1.0, ct.E4M3)]
     dbs = [oracle.dbias(x_cpu), oracle.dbias(-x_cpu)]
