@@ -718,6 +718,17 @@ def secondary(dev, peaks, args) -> dict:
     ms, best = _timed(torch, lambda: ct.fp8_transpose(q, qt))
     res["transpose 16384x12288 FP8"] = _rate_entry(ms, best, 2 * x.numel(), peaks,
                                                    "transpose_fast_kernel")
+    # the cached transpose of lazy transpose caching: with a noop flag, clear then set
+    flag = torch.zeros(1, device=dev)
+    ms, best = _timed(torch, lambda: ct.fp8_transpose(q, qt, noop_flag=flag))
+    res["transpose 16384x12288 FP8, noop flag 0"] = _rate_entry(
+        ms, best, 2 * x.numel(), peaks,
+        "transpose_fast_kernel: a looping first wave over 90% of the tiles, then one tile per CTA")
+    flag.fill_(1.0)
+    ms, best = _timed(torch, lambda: ct.fp8_transpose(q, qt, noop_flag=flag), per_graph=50)
+    res["transpose 16384x12288 FP8, noop flag 1"] = {
+        "us": round(ms * 1e3, 2), "us_best": round(best * 1e3, 2),
+        "note": "the same launch skipped by the flag"}
     del x, q, qt
     # ragged: odd rows and cols (the general kernel)
     x = workloads.normal_bf16(8191, 12287, 1.0, 17, dev)

@@ -73,6 +73,22 @@ def test_transpose_matches_oracle(shape):
     assert np.array_equal(out.numpy().reshape(cols, rows), oracle.fp8_transpose(q_cpu.numpy()))
 
 
+@pytest.mark.parametrize("shape", [(8192, 8192), (4112, 8208), (16, 4096)])
+def test_transpose_with_noop_flag_zero(shape):
+    """With a noop flag (here 0) the aligned transpose runs a looping first
+    wave and one tile per CTA for the rest: 4096 tiles (several per looping
+    CTA), a partial last tile row and column (2145 tiles), and fewer tiles
+    than one wave."""
+    rows, cols = shape
+    g = torch.Generator().manual_seed(rows * 7 + cols)
+    q_cpu = torch.randint(0, 256, (rows, cols), dtype=torch.uint8, generator=g)
+    out = Guarded(rows * cols)
+    ct.fp8_transpose(q_cpu.cuda(), out.t, noop_flag=torch.zeros(1, device="cuda"))
+    torch.cuda.synchronize()
+    out.check()
+    assert np.array_equal(out.numpy().reshape(cols, rows), oracle.fp8_transpose(q_cpu.numpy()))
+
+
 def test_transpose_misaligned():
     q_cpu = torch.randint(0, 256, (256, 256), dtype=torch.uint8)
     big = torch.empty(256 * 256 + 3, dtype=torch.uint8, device="cuda")
