@@ -355,6 +355,7 @@ def run_gpu(args):
     ms_per_step = _max_over_ranks(elapsed_ms / args.steps, world)
 
     e2e = list_e2e(ct, torch, dev, st, args, world)
+    noop_lines = list_noop(ct, torch, dev, st, peaks) if (rank == 0 and args.extra) else {}
     if rank != 0:
         return
     value = aggregate_value(world, STEP_BYTES, ms_per_step)
@@ -426,6 +427,7 @@ def run_gpu(args):
         del st
         torch.cuda.empty_cache()
         line["secondary"] = secondary(dev, peaks, args)
+        line["secondary"].update(noop_lines)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
         line["cpu_baseline_all_cores"] = cpu_baseline_all_cores(seconds=args.cpu_seconds)
@@ -520,6 +522,33 @@ def list_e2e(ct, torch, dev, st, args, world) -> dict:
                     "copied out; copy-in / compute / copy-out on three streams with two buffer "
                     "sets, step i+1's copy-in overlapping step i's copy-out; bound by the host "
                     "link"}
+
+
+def list_noop(ct, torch, dev, st, peaks) -> dict:
+    """The 48-tensor list cast with a noop flag (the FP8 weight copies of
+    lazy refresh: cast once per optimizer step, skipped in the other
+    micro-batches): its rate with the flag at 0 and the skipped launch."""
+    flag = torch.zeros(1, device=dev)
+    res = {}
+
+    def cast():
+        n = LIST_COUNT
+        ct.fp8_multi_cast_transpose(st["xs"], [st["scale"][i:i + 1] for i in range(n)],
+                                    [st["hist"][0, i:i + 1] for i in range(n)],
+                                    [st["tensor_sinv"][i:i + 1] for i in range(n)],
+                                    [o[0] for o in st["outs"]], [o[1] for o in st["outs"]],
+                                    ct.E4M3, noop_flag=flag)
+    ms, best = _timed(torch, cast, iters=3, per_graph=3)
+    res["cast_transpose 48-tensor list, noop flag 0"] = _rate_entry(
+        ms, best, LIST_BYTES, peaks,
+        "direct_loop_kernel (list): a looping first wave over 80% of the tiles, then chunks of "
+        "tiles per group")
+    flag.fill_(1.0)
+    ms, best = _timed(torch, cast, per_graph=50)
+    res["cast_transpose 48-tensor list, noop flag 1"] = {
+        "us": round(ms * 1e3, 2), "us_best": round(best * 1e3, 2),
+        "note": "the same launch skipped by the flag"}
+    return res
 
 
 # ---------------------------------------------------------------------------

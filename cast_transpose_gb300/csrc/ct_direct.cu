@@ -55,6 +55,7 @@ template <bool WRITE_T, bool DBIAS>
 constexpr int tiles_per_cta() { return WRITE_T && !DBIAS ? 2 : 1; }
 
 constexpr int64_t kLoopPercent = 80;
+constexpr int64_t kRestWaves = 8;
 
 
 // The tensor of a list launch that owns global tile `tile`: the last entry
@@ -282,19 +283,35 @@ __global__ void __launch_bounds__(kDirectThreads * TPC, 4 / TPC)
 }
 
 
-// First row and column of tile `tile` of a tensor with `tc` tiles per row.
-__device__ __forceinline__ int2 loop_tile(int tile, int tc) {
-    const int rt = tile / tc;
-    return make_int2(rt * kTileRows, (tile - rt * tc) * kTileCols);
+// Tile `tile` of a launch: the tensor that owns it, its first row and column,
+// and its index within the tensor (0: the tile that writes scale_inv).
+struct LoopPos {
+    int ti, row0, col0, local;
+};
+
+template <int NT>
+__device__ __forceinline__ LoopPos loop_pos(const DirectParams<NT>& p, int tile) {
+    LoopPos r;
+    r.ti = owner(p, tile);
+    const FastTensor& T = p.t[r.ti];
+    r.local = tile - static_cast<int>(T.tile_begin);
+    const int tc = static_cast<int>(T.tile_cols);
+    const int rt = r.local / tc;
+    r.row0 = rt * kTileRows;
+    r.col0 = (r.local - rt * tc) * kTileCols;
+    return r;
 }
 
 // The eight 16-byte loads of one thread (rows rg + 16 * it of column chunk c)
-// of the tile at (row0, col0); rows % 16 == 0, rows and cols below 2^31.
-__device__ __forceinline__ void loop_load(const uint16_t* x, int rows, int cols, int2 t, int c,
-                                          int rg, uint4 (&v)[8]) {
-    const bool col_ok = t.y + 8 * c < cols;
-    const int nr = (rows - t.x) >> 4;   // 16-row blocks left in the tensor
-    const uint16_t* src = x + static_cast<int64_t>(t.x + rg) * cols + t.y + 8 * c;
+// of the tile at `t`; rows % 16 == 0, rows and cols below 2^31.
+template <int NT>
+__device__ __forceinline__ void loop_load(const DirectParams<NT>& p, const LoopPos& t, int c, int rg,
+                                          uint4 (&v)[8]) {
+    const FastTensor& T = p.t[t.ti];
+    const int rows = static_cast<int>(T.rows), cols = static_cast<int>(T.cols);
+    const bool col_ok = t.col0 + 8 * c < cols;
+    const int nr = (rows - t.row0) >> 4;   // 16-row blocks left in the tensor
+    const uint16_t* src = p.x[t.ti] + static_cast<int64_t>(t.row0 + rg) * cols + t.col0 + 8 * c;
 #pragma unroll
     for (int it = 0; it < 8; ++it)
         v[it] = (col_ok && it < nr)
@@ -302,60 +319,63 @@ __device__ __forceinline__ void loop_load(const uint16_t* x, int rows, int cols,
                     : make_uint4(0u, 0u, 0u, 0u);
 }
 
-// Cast + transpose of one tensor (rows % 16 == 0) for calls that pass a
-// noop flag.  Every CTA of the direct kernel starts, waits, reads the flag
-// and exits, so a skipped launch costs about one CTA turnover per tile pair
-// (6.8 us at 16384x12288).  Here the first wave of CTAs (loop_ctas: SMs x 2)
-// loops: group gi of its G = 2 * loop_ctas groups takes tiles gi + k * G for
-// k < loop_tiles, loading tile k + 1 into registers as soon as pass 2 has
-// read tile k out of the shared copy, i.e. during its qT stores.  The CTAs
-// after the first wave take one tile per group from the remainder, as the
-// direct kernel does; the hardware hands them to whichever SM frees a slot
-// first, which evens out SMs that stream slower than others (measured per
-// group on GB300: 5.0 to 6.4 us per tile, so a grid that only loops ends
-// with its slowest SM, 140 against 117 us).
-template <int FMT, int TPC>
+// Cast (+ transpose) for calls that pass a noop flag (rows % 16 == 0, one
+// tensor or a list).  Every CTA of the direct kernel starts, waits, reads
+// the flag and exits, so a skipped launch costs about one CTA turnover per
+// CTA (6.8 us for the 6144 CTAs of 16384x12288).  Here the first wave of
+// CTAs (loop_ctas: SMs x resident CTAs) loops: group gi of its G groups of
+// 256 threads takes tiles gi + k * G for k < loop_tiles, loading tile k + 1
+// into registers as soon as the current one no longer needs them (during
+// its qT stores).  The CTAs after the first wave take rest_chunk
+// consecutive tiles per group from the remainder; the hardware hands them to
+// whichever SM frees a slot first, which evens out SMs that stream slower
+// than others (measured per group on GB300: 5.0 to 6.4 us per tile, so a
+// grid that only loops ends with its slowest SM, 140 against 117 us).
+// Amax is merged per tile, as in the direct kernel.
+template <int NT, int FMT, bool WRITE_T, int TPC>
 __global__ void __launch_bounds__(kDirectThreads * TPC, 4 / TPC)
-    direct_loop_kernel(const __grid_constant__ DirectParams<1> p) {
+    direct_loop_kernel(const __grid_constant__ DirectParams<NT> p) {
     dev::pdl_launch_dependents();
     dev::pdl_wait();
     if (p.noop != nullptr && *p.noop != 0.0f) return;
 
-    __shared__ __align__(16) uint8_t sq_all[TPC][kTileRows * kTileCols];
+    __shared__ __align__(16) uint8_t sq_all[TPC][WRITE_T ? kTileRows * kTileCols : 16];
     __shared__ unsigned s_amax_all[TPC][kDirectWarps];
     const int g = TPC == 1 ? 0 : static_cast<int>(threadIdx.x / kDirectThreads);
     const int tid = threadIdx.x % kDirectThreads, lane = tid & 31, warp = tid >> 5;
     const int total = static_cast<int>(p.total_tiles);
-    // CTAs below loop_ctas: group gi takes tiles gi + k * stride, k < loop_tiles;
-    // the CTAs after them take one tile per group from the remainder.
-    const int stride = p.loop_ctas * TPC;
-    int tile, last;
+    const int groups = p.loop_ctas * TPC;
+    int tile, step, last;
     if (static_cast<int>(blockIdx.x) < p.loop_ctas) {
         tile = static_cast<int>(blockIdx.x) * TPC + g;
-        last = tile + (p.loop_tiles - 1) * stride;
+        step = groups;
+        last = tile + (p.loop_tiles - 1) * step;
     } else {
-        tile = stride * p.loop_tiles + (static_cast<int>(blockIdx.x) - p.loop_ctas) * TPC + g;
-        last = tile;
+        const int u = (static_cast<int>(blockIdx.x) - p.loop_ctas) * TPC + g;
+        tile = groups * p.loop_tiles + u * p.rest_chunk;
+        step = 1;
+        last = tile + p.rest_chunk - 1;
     }
     if (last >= total) last = total - 1;
     if (tile >= total) return;   // a whole group: no barrier involves it
     uint8_t* sq = sq_all[g];
-    const FastTensor& T = p.t[0];
-    const int rows = static_cast<int>(T.rows), cols = static_cast<int>(T.cols);
-    const int tc = static_cast<int>(T.tile_cols);
-    const float scale = *T.scale;
+    unsigned* s_amax = s_amax_all[g];
     const int c = tid & 15, rg = tid >> 4;
     const int b = lane & 7, w = warp * 4 + (lane >> 3);   // pass-2 mapping
 
+    LoopPos cur = loop_pos(p, tile);
     uint4 v[8];
-    loop_load(p.x[0], rows, cols, loop_tile(tile, tc), c, rg, v);
-    uint32_t amax_pair = 0;
+    loop_load(p, cur, c, rg, v);
     for (;;) {
-        int2 t = loop_tile(tile, tc);
+        const FastTensor& T = p.t[cur.ti];
+        const int rows = static_cast<int>(T.rows), cols = static_cast<int>(T.cols);
+        const float scale = *T.scale;
+        const int tfmt = T.fmt;
         {
-            const bool col_ok = t.y + 8 * c < cols;
-            const int nr = (rows - t.x) >> 4;
-            uint8_t* qrow = T.out + static_cast<int64_t>(t.x + rg) * cols + t.y + 8 * c;
+            uint32_t amax_pair = 0;
+            const bool col_ok = cur.col0 + 8 * c < cols;
+            const int nr = (rows - cur.row0) >> 4;
+            uint8_t* qrow = T.out + static_cast<int64_t>(cur.row0 + rg) * cols + cur.col0 + 8 * c;
 #pragma unroll
             for (int it = 0; it < 8; ++it) {
                 const int r = rg + 16 * it;
@@ -363,58 +383,70 @@ __global__ void __launch_bounds__(kDirectThreads * TPC, 4 / TPC)
                 amax_pair = dev::absmax_pair(amax_pair, v[it].y);
                 amax_pair = dev::absmax_pair(amax_pair, v[it].z);
                 amax_pair = dev::absmax_pair(amax_pair, v[it].w);
-                const uint2 q8 = dev::cast8<FMT>(v[it], scale);
+                // FMT < 0: the tensor's own format (uniform over the group)
+                const uint2 q8 = FMT >= 0  ? dev::cast8<FMT < 0 ? 0 : FMT>(v[it], scale)
+                                 : tfmt == 0 ? dev::cast8<0>(v[it], scale)
+                                             : dev::cast8<1>(v[it], scale);
                 if (col_ok && it < nr)
                     __stcs(reinterpret_cast<uint2*>(qrow + static_cast<int64_t>(16 * it) * cols), q8);
-                *reinterpret_cast<uint2*>(sq + r * kTileCols + ((2 * c) ^ dev::swz(r)) * 4) = q8;
+                if constexpr (WRITE_T)
+                    *reinterpret_cast<uint2*>(sq + r * kTileCols + ((2 * c) ^ dev::swz(r)) * 4) = q8;
             }
+            const unsigned m = __reduce_max_sync(0xFFFFFFFFu, dev::pair_to_f32_bits(amax_pair));
+            if (lane == 0) s_amax[warp] = m;
         }
+        const int next = tile + step;
         tile_sync<TPC>(g);
-        if (tile == 0 && tid == 0) *T.scale_inv = __fdiv_rn(1.0f, scale);
-
-        uint32_t o[4][4];
-        {
-            const uint32_t* sq32 = reinterpret_cast<const uint32_t*>(sq);
-            uint32_t rw[16];
+        if (tid == 0) {
+            unsigned a = s_amax[0];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int r = 16 * b + j;
-                rw[j] = sq32[r * (kTileCols / 4) + (w ^ dev::swz(r))];
+            for (int k = 1; k < kDirectWarps; ++k) a = a > s_amax[k] ? a : s_amax[k];
+            if (a != 0) atomicMax(reinterpret_cast<unsigned*>(T.amax), a);
+            if (cur.local == 0) *T.scale_inv = __fdiv_rn(1.0f, scale);
+        }
+        LoopPos nxt = cur;
+        if constexpr (WRITE_T) {
+            uint32_t o[4][4];
+            {
+                const uint32_t* sq32 = reinterpret_cast<const uint32_t*>(sq);
+                uint32_t rw[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int r = 16 * b + j;
+                    rw[j] = sq32[r * (kTileCols / 4) + (w ^ dev::swz(r))];
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    dev::transpose4x4(rw[4 * k], rw[4 * k + 1], rw[4 * k + 2], rw[4 * k + 3],
+                                      o[0][k], o[1][k], o[2][k], o[3][k]);
+            }
+            // qT columns 0-1 of the block, the next tile's loads, columns 2-3
+            const bool row_ok = cur.row0 + 16 * b < rows;
+            uint8_t* dst = T.out_t + static_cast<int64_t>(cur.col0 + 4 * w) * rows + cur.row0 + 16 * b;
+#pragma unroll
+            for (int kq = 0; kq < 2; ++kq)
+                if (row_ok && cur.col0 + 4 * w + kq < cols)
+                    __stcs(reinterpret_cast<uint4*>(dst + static_cast<int64_t>(kq) * rows),
+                           make_uint4(o[kq][0], o[kq][1], o[kq][2], o[kq][3]));
+            if (next <= last) {
+                nxt = loop_pos(p, next);
+                loop_load(p, nxt, c, rg, v);
             }
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                dev::transpose4x4(rw[4 * k], rw[4 * k + 1], rw[4 * k + 2], rw[4 * k + 3], o[0][k],
-                                  o[1][k], o[2][k], o[3][k]);
+            for (int kq = 2; kq < 4; ++kq)
+                if (row_ok && cur.col0 + 4 * w + kq < cols)
+                    __stcs(reinterpret_cast<uint4*>(dst + static_cast<int64_t>(kq) * rows),
+                           make_uint4(o[kq][0], o[kq][1], o[kq][2], o[kq][3]));
+        } else {
+            if (next <= last) {
+                nxt = loop_pos(p, next);
+                loop_load(p, nxt, c, rg, v);
+            }
         }
-        // qT columns 0-1 of the block, the next tile's loads, columns 2-3
-        const bool row_ok = t.x + 16 * b < rows;
-        uint8_t* dst = T.out_t + static_cast<int64_t>(t.y + 4 * w) * rows + t.x + 16 * b;
-        const int next = tile + stride;
-#pragma unroll
-        for (int kq = 0; kq < 2; ++kq)
-            if (row_ok && t.y + 4 * w + kq < cols)
-                __stcs(reinterpret_cast<uint4*>(dst + static_cast<int64_t>(kq) * rows),
-                       make_uint4(o[kq][0], o[kq][1], o[kq][2], o[kq][3]));
-        if (next <= last) loop_load(p.x[0], rows, cols, loop_tile(next, tc), c, rg, v);
-#pragma unroll
-        for (int kq = 2; kq < 4; ++kq)
-            if (row_ok && t.y + 4 * w + kq < cols)
-                __stcs(reinterpret_cast<uint4*>(dst + static_cast<int64_t>(kq) * rows),
-                       make_uint4(o[kq][0], o[kq][1], o[kq][2], o[kq][3]));
         if (next > last) break;
         tile = next;
-        tile_sync<TPC>(g);   // every thread has read the copy before it is rewritten
-    }
-
-    unsigned* s_amax = s_amax_all[g];
-    const unsigned m = __reduce_max_sync(0xFFFFFFFFu, dev::pair_to_f32_bits(amax_pair));
-    if (lane == 0) s_amax[warp] = m;
-    tile_sync<TPC>(g);
-    if (tid == 0) {
-        unsigned a = s_amax[0];
-#pragma unroll
-        for (int k = 1; k < kDirectWarps; ++k) a = a > s_amax[k] ? a : s_amax[k];
-        if (a != 0) atomicMax(reinterpret_cast<unsigned*>(T.amax), a);
+        cur = nxt;
+        tile_sync<TPC>(g);   // the shared copy and the amax slots are rewritten next
     }
 }
 
@@ -456,6 +488,17 @@ cudaError_t launch_tpc(const DirectParams<NT>& p, cudaStream_t stream) {
                       stream, p);
 }
 
+// The looping kernel's index arithmetic is in 32 bits, and its loads take
+// whole 16-row blocks.
+template <int NT>
+bool loop_fits(const DirectParams<NT>& p) {
+    for (int i = 0; i < p.n; ++i) {
+        const FastTensor& T = p.t[i];
+        if (T.rows % 16 != 0 || T.rows >= INT_MAX || T.cols >= INT_MAX) return false;
+    }
+    return true;
+}
+
 template <int NT, int FMT, bool WRITE_T, bool DBIAS>
 cudaError_t launch_one(const DirectParams<NT>& p, cudaStream_t stream) {
     if (p.total_tiles <= 0 || p.total_tiles > INT_MAX) return cudaErrorInvalidValue;
@@ -466,22 +509,31 @@ cudaError_t launch_one(const DirectParams<NT>& p, cudaStream_t stream) {
     if constexpr (NT == 1 && TPC != 1)
         if (p.t[0].rows % 16 != 0) return launch_tpc<NT, FMT, WRITE_T, DBIAS, 1>(p, stream);
     // Calls with a noop flag: the looping first wave covers kLoopPercent of
-    // the tiles.  Measured at 16384x12288 on GB300, flag 0 / flag 1:
-    // 60% 6.81 TB/s / 3.4 us, 70% 6.78 / 2.9, 80% 6.75 / 2.25, 90% 6.60 / 1.6;
-    // the direct kernel 6.90 TB/s / 6.8 us.
-    if constexpr (NT == 1 && TPC == 2 && FMT >= 0) {
+    // the tiles.  Measured for 16384x12288 cast + transpose on GB300, flag 0 /
+    // flag 1: 60% 6.81 TB/s / 3.4 us, 70% 6.78 / 2.9, 80% 6.75 / 2.25, 90%
+    // 6.60 / 1.6; the direct kernel 6.90 TB/s / 6.8 us.  The remainder goes in
+    // chunks of rest_chunk tiles per group, sized so that it spans about
+    // kRestWaves waves of groups (one tile per group at 16384x12288; a list
+    // of 300 K tiles would otherwise start 30 K CTAs to skip).
+    if constexpr (!DBIAS) {
         const int sms = sm_count();
-        if (p.noop != nullptr && !p.x_ready && sms > 0 && p.t[0].rows < INT_MAX &&
-            p.t[0].cols < INT_MAX && p.total_tiles < INT_MAX / 2) {
-            DirectParams<1> q = p;
+        if (p.noop != nullptr && !p.x_ready && sms > 0 && p.total_tiles < INT_MAX / 2 &&
+            loop_fits(p)) {
+            DirectParams<NT> q = p;
             q.loop_ctas = sms * (4 / TPC);
             const int64_t groups = static_cast<int64_t>(q.loop_ctas) * TPC;
-            q.loop_tiles = static_cast<int>(p.total_tiles * kLoopPercent / 100 / groups);
-            if (q.loop_tiles < 1) q.loop_tiles = 1;
-            const int64_t rest = p.total_tiles - groups * q.loop_tiles;
-            const int64_t grid = q.loop_ctas + (rest > 0 ? (rest + TPC - 1) / TPC : 0);
+            int64_t lt = p.total_tiles * kLoopPercent / 100 / groups;
+            if (lt < 1) lt = 1;
+            q.loop_tiles = static_cast<int>(lt);
+            const int64_t rest = p.total_tiles - groups * lt;
+            int64_t chunk = rest / (kRestWaves * groups);
+            if (chunk < 1) chunk = 1;
+            q.rest_chunk = static_cast<int>(chunk);
+            q.prefetch_ctas = 0;
+            const int64_t units = rest > 0 ? (rest + chunk - 1) / chunk : 0;
+            const int64_t grid = q.loop_ctas + (units + TPC - 1) / TPC;
             const dim3 g(static_cast<unsigned>(grid)), b(kDirectThreads * TPC);
-            return launch_pdl(direct_loop_kernel<FMT, TPC>, g, b, 0, stream, q);
+            return launch_pdl(direct_loop_kernel<NT, FMT, WRITE_T, TPC>, g, b, 0, stream, q);
         }
     }
     return launch_tpc<NT, FMT, WRITE_T, DBIAS, TPC>(p, stream);

@@ -111,8 +111,9 @@ struct DirectParams {
     int x_ready;            // caller's promise: no kernel still running writes x
                             // (the tiles may be loaded before the dependency wait)
     int prefetch_ctas;      // CTAs (from block 0) that prefetch their tile into L2 before the wait
-    int loop_ctas;          // looping launches: CTAs that loop over loop_tiles tiles per group
-    int loop_tiles;
+    int loop_ctas;          // looping launches: CTAs that loop over loop_tiles tiles per group,
+    int loop_tiles;         // then rest_chunk consecutive tiles per group for the CTAs after them
+    int rest_chunk;
 };
 constexpr int64_t kDirectMinTiles = 2048;
 // `variant`: 0 = cast + transpose, 1 = cast only; `dbias` requires variant 0.

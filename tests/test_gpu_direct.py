@@ -63,6 +63,23 @@ def test_all_bf16_patterns_tiled():
 
 
 @pytest.mark.parametrize("fmt", [ct.E4M3, ct.E5M2])
+@pytest.mark.parametrize("shape", RAGGED)
+def test_cast_only_noop_flag_zero(fmt, shape):
+    """A plain cast given a noop flag (here 0) takes the looping grid too."""
+    rows, cols = shape
+    x_cpu = workloads.normal_bf16(rows, cols, 30.0, 43 + rows)
+    q = Guarded(rows * cols)
+    s, a, si = scalar(0.75), scalar(0.0), scalar(0.0)
+    ct.fp8_cast(x_cpu.cuda(), s, a, si, q.t, fmt, noop_flag=scalar(0.0))
+    torch.cuda.synchronize()
+    q.check()
+    ref = oracle.cast_transpose(x_cpu, 0.75, fmt, want_qt=False)
+    assert np.array_equal(q.numpy().reshape(rows, cols), ref["q"])
+    assert f32_bits(a.item()) == f32_bits(ref["amax"])
+    assert f32_bits(si.item()) == f32_bits(ref["scale_inv"])
+
+
+@pytest.mark.parametrize("fmt", [ct.E4M3, ct.E5M2])
 def test_ragged_cast_only(fmt):
     rows, cols = RAGGED[0]
     x_cpu = workloads.normal_bf16(rows, cols, 30.0, 41)
@@ -113,10 +130,13 @@ def test_dbias_deterministic():
     assert np.array_equal(outs[0], outs[1])
 
 
+@pytest.mark.parametrize("noop", [None, 0.0])
 @pytest.mark.parametrize("per_tensor_fmt", [False, True])
-def test_list_launch(per_tensor_fmt):
+def test_list_launch(per_tensor_fmt, noop):
     """One list launch of >= 2048 tiles: ragged entries, a one-tile-row entry,
-    and one entry that takes the general kernel (33 x 65)."""
+    and one entry that takes the general kernel (33 x 65).  With a noop flag
+    (here 0) the list takes the looping grid: tiles of different tensors in
+    one group's run."""
     shapes = [(4112, 1040), (2048, 2064), (16, 4096), (1024, 4096), (1040, 4096), (33, 65),
               (4096, 4096), (144, 272)]
     fmts = [ct.E4M3, ct.E5M2, ct.E5M2, ct.E4M3, ct.E5M2, ct.E4M3, ct.E4M3, ct.E5M2]
@@ -133,10 +153,11 @@ def test_list_launch(per_tensor_fmt):
     args = ([x.cuda() for x in xs_cpu], [scales[i:i + 1] for i in range(n)],
             [amax[i:i + 1] for i in range(n)], [sinv[i:i + 1] for i in range(n)],
             [o.t for o in outs], [o.t for o in outs_t])
+    flag = None if noop is None else scalar(noop)
     if per_tensor_fmt:
-        ct.fp8_multi_cast_transpose_ex(*args, fmts)
+        ct.fp8_multi_cast_transpose_ex(*args, fmts, noop_flag=flag)
     else:
-        ct.fp8_multi_cast_transpose(*args, ct.E4M3)
+        ct.fp8_multi_cast_transpose(*args, ct.E4M3, noop_flag=flag)
     torch.cuda.synchronize()
     a, si = amax.cpu().numpy(), sinv.cpu().numpy()
     for i, x in enumerate(xs_cpu):
