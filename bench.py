@@ -759,6 +759,14 @@ def secondary(dev, peaks, args) -> dict:
         "us": round(ms * 1e3, 2), "us_best": round(best * 1e3, 2),
         "note": "the same launch skipped by the flag"}
     del x, q, qt
+    # an odd token count: rows % 16 != 0, cols a multiple of 128 (the direct
+    # kernel, transposed blocks at a different offset in every column)
+    x = workloads.normal_bf16(8191, 12288, 1.0, 17, dev)
+    q, qt = ct.empty_outputs(x)
+    ms, best = _timed(torch, lambda: ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3))
+    res["cast_transpose 8191x12288 E4M3 (odd rows)"] = _rate_entry(
+        ms, best, 4 * x.numel() + 12, peaks, "direct_cast_transpose_kernel (odd-row stores)")
+    del x, q, qt
     # ragged: odd rows and cols (the general kernel)
     x = workloads.normal_bf16(8191, 12287, 1.0, 17, dev)
     q, qt = ct.empty_outputs(x)
@@ -1016,6 +1024,8 @@ def profile_case(name: str) -> None:
                     FP8 transposes of its q (the general kernels);
       'flat':       three plain casts of the ragged 8191x12287 matrix (the flat
                     cast kernel);
+      'odd':        cast-transpose of an 8191x12288 matrix (rows % 16 != 0:
+                    the direct kernel's odd-row stores);
       'loop':       the same with a noop flag at 0 (the looping grid that calls
                     with a noop flag take);
       'noop':       three launches of the activation cast-transpose with the
@@ -1060,6 +1070,11 @@ def profile_case(name: str) -> None:
             ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3)
         for _ in range(3):
             ct.fp8_transpose(q, qt)
+    elif name == "odd":
+        x = workloads.normal_bf16(8191, 12288, 1.0, 17, dev)
+        q, qt = ct.empty_outputs(x)
+        for _ in range(3):
+            ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3)
     elif name == "flat":
         x = workloads.normal_bf16(8191, 12287, 1.0, 17, dev)
         q, qt = ct.empty_outputs(x)
@@ -1108,7 +1123,7 @@ def _parse(argv=None):
     ap.add_argument("--extra", action=argparse.BooleanOptionalAction, default=True,
                     help="also time the secondary workloads")
     ap.add_argument("--profile-case",
-                    choices=["activation", "gradient", "list", "cast", "general", "flat",
+                    choices=["activation", "gradient", "list", "cast", "general", "flat", "odd",
                              "loop", "noop", "weight"],
                     default=None,
                     help="only run 3 launches of one workload's kernel (for ncu) and exit")

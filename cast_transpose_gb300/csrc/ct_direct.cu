@@ -84,12 +84,110 @@ __device__ __forceinline__ void tile_sync(int g) {
 using dev::colsum_index;
 using dev::kColsumStride;
 
+// Transposed stores when rows % 16 != 0.  The qT segment of column j of a
+// tile (rows row0 .. row0 + 127) then starts a_j = (col * rows + row0) % 16
+// bytes into a 16-byte block, a different offset for every column.  The
+// tile instead owns the rows [row0 - a_j, row0 + 128 - a_j) of column j:
+// eight whole aligned 16-byte blocks, the first of which holds the last a_j
+// rows of the tile above (the halo: its last 16 rows are loaded, cast and
+// transposed with the tile).  Pass 2 writes the transposed bytes into a
+// column-major copy (kOddPitch bytes per column: 16 halo rows, then the
+// tile's 128); a third pass reads each block back at its offset (five 4-byte
+// loads, four funnel shifts) and stores it with one 16-byte store.  The first
+// tile row owns [0, 128 - a_j) and the last [row0 - a_j, rows): their blocks
+// at the column ends are stored masked.
+constexpr int kHaloRows = 16;
+constexpr int kOddPitch = kHaloRows + kTileRows;
+
+// Word wd of halo row h (0 .. 15, copy row 128 + h) lives at wd ^ halo_swz(h):
+// the 8 lanes that read one word from rows 2b, 2b + 1 (b = 0 .. 7) then hit 8
+// distinct groups of 4 banks, and every 8-byte row store stays whole.
+__device__ __forceinline__ int halo_swz(int h) { return 4 * ((h >> 1) & 7); }
+
+// Passes 2 (end) and 3 of the odd-row path, per warp: warp W transposes
+// the 4-column words 4W .. 4W + 3, i.e. columns 16W .. 16W + 15, and stores
+// exactly those columns' blocks, so it synchronises with itself only.
+// o: the thread's transposed pieces (rows 16b .. 16b + 15 of columns
+// 4w .. 4w + 3); sq32: the row-major copy, halo rows at 128 .. 143; sqt: the
+// column-major copy.
+__device__ __forceinline__ void odd_transpose_stores(const FastTensor& T, int64_t rt, int64_t row0,
+                                                     int64_t col0, const uint32_t* sq32,
+                                                     const uint32_t (&o)[4][4], int b, int w,
+                                                     int lane, int warp, uint8_t* sqt) {
+    const int64_t rows = T.rows, cols = T.cols;
+#pragma unroll
+    for (int kq = 0; kq < 4; ++kq)
+        *reinterpret_cast<uint4*>(sqt + (4 * w + kq) * kOddPitch + kHaloRows + 16 * b) =
+            make_uint4(o[kq][0], o[kq][1], o[kq][2], o[kq][3]);
+    if (rt > 0) {   // halo rows 2b and 2b + 1 of word w: two bytes of each of its columns
+        const int r0 = kTileRows + 2 * b, r1 = r0 + 1;
+        const uint32_t h0 = sq32[r0 * (kTileCols / 4) + (w ^ halo_swz(2 * b))];
+        const uint32_t h1 = sq32[r1 * (kTileCols / 4) + (w ^ halo_swz(2 * b + 1))];
+#pragma unroll
+        for (int kq = 0; kq < 4; ++kq)
+            *reinterpret_cast<uint16_t*>(sqt + (4 * w + kq) * kOddPitch + 2 * b) =
+                static_cast<uint16_t>(__byte_perm(h0, h1, kq | ((4 + kq) << 4)));
+    }
+    __syncwarp();
+
+    // a_j = (a0 + j * d) % 16 for column j of the tile
+    const int d = static_cast<int>(rows & 15);
+    const int a0 =
+        static_cast<int>((reinterpret_cast<uintptr_t>(T.out_t) + col0 * rows + row0) & 15);
+    const int k = lane & 7, g4 = lane >> 3;   // block k of column group g4
+    const bool last = row0 + kTileRows >= rows;
+    if (rt > 0 && !last) {
+        // The 4 columns of one store instruction lie sigma = 2^lsig apart,
+        // sigma such that their a_j differ by 4 (mod 16), so that their 4-byte
+        // loads fall in 4 distinct bank classes (d = 8 excepted: 2-way).
+        const int lsig = (d & 1) ? 2 : (d & 2) ? 1 : 0;
+        const int jb = 16 * warp + (g4 << lsig);
+        const int ab = a0 + jb * d;
+        uint8_t* const dst = T.out_t + (col0 + jb) * rows + row0 + 16 * k;
+        const uint8_t* const src = sqt + jb * kOddPitch + kHaloRows + 16 * k;
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int dj = ((it >> lsig) << (lsig + 2)) + (it & ((1 << lsig) - 1));
+            const int aj = (ab + dj * d) & 15;
+            const int s = dj * kOddPitch - aj;   // the block's first byte, from src
+            const uint32_t* p = reinterpret_cast<const uint32_t*>(src + (s & ~3));
+            const int sh = 8 * (s & 3);
+            const uint32_t w0 = p[0], w1 = p[1], w2 = p[2], w3 = p[3], w4 = p[4];
+            if (col0 + jb + dj < cols)
+                __stcs(reinterpret_cast<uint4*>(dst + dj * rows - aj),
+                       make_uint4(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh),
+                                  __funnelshift_r(w2, w3, sh), __funnelshift_r(w3, w4, sh)));
+        }
+    } else {   // first or last tile row: blocks 0 .. 8, cut to the rows the tile owns
+        const int L = static_cast<int>(last ? rows - row0 : kTileRows);
+        for (int e = lane; e < 16 * 9; e += 32) {
+            const int jq = e / 9, kk = e - 9 * jq, j = 16 * warp + jq;
+            if (col0 + j >= cols) continue;
+            const int aj = (a0 + j * d) & 15;
+            const int blk_row = 16 * kk - aj;   // tile row of the block's first byte
+            const int own_lo = rt > 0 ? -aj : 0, own_hi = last ? L : kTileRows - aj;
+            const int lo = max(0, own_lo - blk_row), hi = min(16, own_hi - blk_row);
+            if (lo >= hi) continue;
+            const int s = kHaloRows + blk_row;
+            const uint32_t* p = reinterpret_cast<const uint32_t*>(sqt + j * kOddPitch + (s & ~3));
+            const int sh = 8 * (s & 3);
+            const uint32_t v[4] = {__funnelshift_r(p[0], p[1], sh), __funnelshift_r(p[1], p[2], sh),
+                                   __funnelshift_r(p[2], p[3], sh), __funnelshift_r(p[3], p[4], sh)};
+            uint8_t* blk = T.out_t + (col0 + j) * rows + row0 + blk_row;
+            if (lo == 0 && hi == 16) __stcs(reinterpret_cast<uint4*>(blk), make_uint4(v[0], v[1], v[2], v[3]));
+            else gen::store_range(blk, v, lo, hi);
+        }
+    }
+}
+
 // EARLY: the launch issues work before the wait for the preceding kernel
 // (x_ready loads, or first-wave L2 prefetches); without it the kernel is
-// compiled without that path.
-template <int NT, int FMT, bool WRITE_T, bool DBIAS, int TPC, bool EARLY>
+// compiled without that path.  ODD: rows % 16 != 0 (one tensor, one tile per
+// CTA, with the transpose); otherwise rows % 16 == 0.
+template <int NT, int FMT, bool WRITE_T, bool DBIAS, int TPC, bool EARLY, bool ODD>
 __global__ void __launch_bounds__(kDirectThreads * TPC, 4 / TPC)
     direct_cast_transpose_kernel(const __grid_constant__ DirectParams<NT> p) {
+    static_assert(!ODD || (NT == 1 && TPC == 1 && WRITE_T), "the odd-row path is single-tile");
     // The next kernel of the stream may be scheduled as soon as this grid's
     // last wave is resident; it waits for this grid on the device.
     dev::pdl_launch_dependents();
@@ -102,9 +200,12 @@ __global__ void __launch_bounds__(kDirectThreads * TPC, 4 / TPC)
         if (p.noop != nullptr && *p.noop != 0.0f) return;
     }
 
-    __shared__ __align__(16) uint8_t sq_all[TPC][WRITE_T ? kTileRows * kTileCols : 16];
+    __shared__ __align__(16) uint8_t
+        sq_all[TPC][WRITE_T ? (kTileRows + (ODD ? kHaloRows : 0)) * kTileCols : 16];
     __shared__ __align__(16) float colsum_all[TPC][DBIAS ? kDirectWarps * kColsumStride : 4];
     __shared__ unsigned s_amax_all[TPC][kDirectWarps];
+    // ODD: the column-major copy, and room for the last column's fifth word
+    __shared__ __align__(16) uint8_t sqt[ODD ? kTileCols * kOddPitch + 32 : 16];
 
     // Tile coordinates come from the launch parameters only, so they are
     // known before the dependency wait.
@@ -193,6 +294,10 @@ __global__ void __launch_bounds__(kDirectThreads * TPC, 4 / TPC)
                                            : make_uint4(0u, 0u, 0u, 0u);
         }
     }
+    uint4 vh = make_uint4(0u, 0u, 0u, 0u);   // ODD: row row0 - 16 + rg of the halo
+    if constexpr (ODD) {
+        if (rt > 0 && col_ok && (rows & 15) != 8) vh = __ldcs(reinterpret_cast<const uint4*>(xin + (row0 - kHaloRows + rg) * cols));
+    }
 
     uint32_t amax_pair = 0;
     float cs[8];
@@ -219,6 +324,11 @@ __global__ void __launch_bounds__(kDirectThreads * TPC, 4 / TPC)
         if (col_ok && row0 + r < rows) __stcs(reinterpret_cast<uint2*>(qrow + r * cols), q8);
         if constexpr (WRITE_T)   // words 2c, 2c+1 of row r
             *reinterpret_cast<uint2*>(sq + r * kTileCols + ((2 * c) ^ dev::swz(r)) * 4) = q8;
+    }
+    if constexpr (ODD) {   // the halo rows go to rows 128 .. 143 of the copy
+        const int r = kTileRows + rg;
+        *reinterpret_cast<uint2*>(sq + r * kTileCols + ((2 * c) ^ halo_swz(rg)) * 4) =
+            dev::cast8<FMT < 0 ? 0 : FMT>(vh, scale);
     }
     const unsigned m = __reduce_max_sync(0xFFFFFFFFu, dev::pair_to_f32_bits(amax_pair));
     if (lane == 0) s_amax[warp] = m;
@@ -260,8 +370,8 @@ __global__ void __launch_bounds__(kDirectThreads * TPC, 4 / TPC)
         for (int g = 0; g < 4; ++g)
             dev::transpose4x4(rw[4 * g], rw[4 * g + 1], rw[4 * g + 2], rw[4 * g + 3], o[0][g],
                               o[1][g], o[2][g], o[3][g]);
-        const int64_t row = row0 + 16 * b;
-        if ((rows & 15) == 0) {   // whole, 16-byte aligned blocks
+        if constexpr (!ODD) {   // rows % 16 == 0: whole, 16-byte aligned blocks
+            const int64_t row = row0 + 16 * b;
             if (row < rows) {
 #pragma unroll
                 for (int kq = 0; kq < 4; ++kq) {
@@ -271,17 +381,21 @@ __global__ void __launch_bounds__(kDirectThreads * TPC, 4 / TPC)
                                make_uint4(o[kq][0], o[kq][1], o[kq][2], o[kq][3]));
                 }
             }
-        } else {   // rows % 16 != 0: each column's segment of qT starts at any byte
+        } else if ((rows & 15) == 8) {
+            // every column's segment starts 0 or 8 bytes into a block: its
+            // neighbouring-lane pieces and 8-byte edge stores cost less
+            // than the halo (6.23 against 5.85 TB/s on 8200x12288)
             const int L = static_cast<int>(rows - row0 < kTileRows ? rows - row0 : kTileRows);
 #pragma unroll
             for (int kq = 0; kq < 4; ++kq) {
                 const int64_t col = col0 + 4 * w + kq;
                 gen::store_segment_x8(T.out_t + col * rows + row0, col < cols ? L : 0, o[kq], b);
             }
+        } else {
+            odd_transpose_stores(T, rt, row0, col0, sq32, o, b, w, lane, warp, sqt);
         }
     }
 }
-
 
 // Tile `tile` of a launch: the tensor that owns it, its first row and column,
 // and its index within the tensor (0: the tile that writes scale_inv).
@@ -465,7 +579,7 @@ int sm_count() {
     return cache[dev];
 }
 
-template <int NT, int FMT, bool WRITE_T, bool DBIAS, int TPC>
+template <int NT, int FMT, bool WRITE_T, bool DBIAS, int TPC, bool ODD = false>
 cudaError_t launch_tpc(const DirectParams<NT>& p, cudaStream_t stream) {
     const int64_t grid = (p.total_tiles + TPC - 1) / TPC;
     // The first wave (SMs x resident CTAs) prefetches its tiles, and the
@@ -481,10 +595,10 @@ cudaError_t launch_tpc(const DirectParams<NT>& p, cudaStream_t stream) {
         DirectParams<1> q = p;
         q.prefetch_ctas = (TPC == 1 && p.noop == nullptr) ? sm_count() * 4 : 0;
         if (q.x_ready || q.prefetch_ctas > 0)
-            return launch_pdl(direct_cast_transpose_kernel<1, FMT, WRITE_T, DBIAS, TPC, true>, g, b,
+            return launch_pdl(direct_cast_transpose_kernel<1, FMT, WRITE_T, DBIAS, TPC, true, ODD>, g, b,
                               0, stream, q);
     }
-    return launch_pdl(direct_cast_transpose_kernel<NT, FMT, WRITE_T, DBIAS, TPC, false>, g, b, 0,
+    return launch_pdl(direct_cast_transpose_kernel<NT, FMT, WRITE_T, DBIAS, TPC, false, ODD>, g, b, 0,
                       stream, p);
 }
 
@@ -506,8 +620,8 @@ cudaError_t launch_one(const DirectParams<NT>& p, cudaStream_t stream) {
     // rows % 16 != 0 (single tensors only): 1 tile per CTA, measured faster
     // for the transposed stores at any alignment (4.85 against 4.08 TB/s on
     // 8191x12288)
-    if constexpr (NT == 1 && TPC != 1)
-        if (p.t[0].rows % 16 != 0) return launch_tpc<NT, FMT, WRITE_T, DBIAS, 1>(p, stream);
+    if constexpr (NT == 1)
+        if (p.t[0].rows % 16 != 0) return launch_tpc<NT, FMT, WRITE_T, DBIAS, 1, WRITE_T>(p, stream);
     // Calls with a noop flag: the looping first wave covers kLoopPercent of
     // the tiles.  Measured for 16384x12288 cast + transpose on GB300, flag 0 /
     // flag 1: 60% 6.81 TB/s / 3.4 us, 70% 6.78 / 2.9, 80% 6.75 / 2.25, 90%

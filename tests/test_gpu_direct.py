@@ -348,6 +348,54 @@ def test_rows_not_multiple_of_16(fmt, shape):
     assert f32_bits(a.item()) == f32_bits(ref["amax"])
 
 
+@pytest.mark.parametrize("d", range(1, 16))
+def test_odd_rows_every_residue(d):
+    """rows % 16 = d, for every d: an interior tile row stores whole aligned
+    16-byte blocks of qT, the first of which starts up to 15 rows above the
+    tile (rows of the tile above, loaded with it); the first and last tile
+    rows are cut at the column ends.  Five tile rows, three interior; 264
+    columns leave a ragged column tile.  Cast-transpose eager, with a noop
+    flag 0 (E4M3) and with x_ready (E5M2); dbias; a noop flag 1 writes
+    nothing."""
+    rows, cols = 512 + 128 + d, 264
+    x_cpu = workloads.normal_bf16(rows, cols, 20.0, 300 + d)
+    ref4 = oracle.cast_transpose(x_cpu, 1.5, ct.E4M3)
+    assert_same_cast(cast_transpose_gpu(x_cpu.cuda(), 1.5, ct.E4M3), ref4)
+    assert_same_cast(cast_transpose_gpu(x_cpu.cuda(), 1.5, ct.E4M3, noop=scalar(0.0)), ref4)
+    x = x_cpu.cuda()
+    n = rows * cols
+    q, qt = Guarded(n), Guarded(n)
+    s, a, si = scalar(1.5), scalar(0.0), scalar(0.0)
+    ct.fp8_cast_transpose(x, s, a, si, q.t, qt.t, ct.E5M2, x_ready=True)
+    torch.cuda.synchronize()
+    q.check()
+    qt.check()
+    ref5 = oracle.cast_transpose(x_cpu, 1.5, ct.E5M2)
+    assert np.array_equal(q.numpy().reshape(rows, cols), ref5["q"])
+    assert np.array_equal(qt.numpy().reshape(cols, rows), ref5["qt"])
+    q2, qt2 = Guarded(n), Guarded(n)
+    db = Guarded(cols, dtype=torch.float32)
+    ws = torch.empty(ct.dbias_workspace_size(rows, cols), dtype=torch.uint8, device="cuda")
+    ct.fp8_dbias_cast_transpose(x, scalar(1.5), scalar(0.0), scalar(0.0), q2.t, qt2.t, db.t, ws,
+                                ct.E4M3)
+    torch.cuda.synchronize()
+    for g in (q2, qt2, db):
+        g.check()
+    assert np.array_equal(q2.numpy().reshape(rows, cols), ref4["q"])
+    assert np.array_equal(qt2.numpy().reshape(cols, rows), ref4["qt"])
+    assert dbias_tolerance_ok(db.numpy(), oracle.dbias(x_cpu), x_cpu)
+    q3, qt3 = Guarded(n), Guarded(n)
+    q3.t.fill_(0x5A)
+    qt3.t.fill_(0x5A)
+    a3 = scalar(0.0)
+    ct.fp8_cast_transpose(x, scalar(1.5), a3, scalar(0.0), q3.t, qt3.t, ct.E4M3,
+                          noop_flag=scalar(1.0))
+    torch.cuda.synchronize()
+    q3.check()
+    qt3.check()
+    assert (q3.numpy() == 0x5A).all() and (qt3.numpy() == 0x5A).all() and a3.item() == 0.0
+
+
 @pytest.mark.parametrize("rows", [8192, 4096])
 def test_default_path_sees_x_written_by_the_preceding_kernel(rows):
     """The direct kernel's first wave asks for its tiles, and the second
