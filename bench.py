@@ -588,7 +588,9 @@ def weight_step(dev, peaks, steps) -> dict:
     """The weight-like 4096x4096 step: eight casts of x * 2^k (k = -4..3,
     resident copies), each followed by the scale update, in one CUDA graph;
     with CT_X_READY (the update before each cast writes only fp32 scalars)
-    and on the default path.  Per-kernel spans come from external event
+    and on the default path; then the same two with the updates deferred
+    (fp8_cast_transpose_pending, one fp8_amax_and_scale_update_pending per
+    step: the same results).  Per-kernel spans come from external event
     nodes on a side branch of an evented copy of the graph."""
     import torch
 
@@ -619,19 +621,33 @@ def weight_step(dev, peaks, steps) -> dict:
                 with torch.cuda.stream(side):
                     ev[2 + 2 * k].record()
 
+    pend = torch.zeros(len(xs), 1, device=dev)
+
+    def step_deferred(x_ready):
+        # the same step with the 8 updates deferred: each cast derives the
+        # scale the updates before it would have set, one update pass at the end
+        for k, x in enumerate(xs):
+            ct.fp8_cast_transpose_pending(x, hist, scale, pend, 0, k, tensor_sinv[k:k + 1],
+                                          outs[k][0], outs[k][1], ct.E4M3, x_ready=x_ready)
+        ct.fp8_amax_and_scale_update_pending(hist, scale, recipe_sinv, pend, ct.E4M3)
+
     s = torch.cuda.Stream(device=dev)
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
         step(True)
+        step_deferred(True)
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
     res = {"workload": "weight-like bf16 4096x4096 N(0,0.02) x 2^k, k=-4..3: per step 8 x (E4M3 "
                        "cast+transpose+amax, then the update, L=16, margin 0), one CUDA graph",
            "bytes_per_step": step_bytes}
-    for x_ready in (True, False):
+    variants = (("x_ready", lambda: step(True)), ("default_path", lambda: step(False)),
+                ("deferred_updates_x_ready", lambda: step_deferred(True)),
+                ("deferred_updates_default_path", lambda: step_deferred(False)))
+    for key, fn in variants:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            step(x_ready)
+            fn()
         for _ in range(5):
             g.replay()
         torch.cuda.synchronize()
@@ -643,7 +659,6 @@ def weight_step(dev, peaks, steps) -> dict:
         b.record()
         torch.cuda.synchronize()
         ms = a.elapsed_time(b) / n
-        key = "x_ready" if x_ready else "default_path"
         res[key] = {"us_per_step": round(ms * 1e3, 2),
                     "GB/s": round(step_bytes / ms / 1e6, 1),
                     "pct_of_nominal_8000_gbs": _pct_nominal(step_bytes / ms / 1e6)}

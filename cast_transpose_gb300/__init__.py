@@ -87,6 +87,11 @@ def lib() -> ctypes.CDLL:
             L.fp8_amax_and_scale_update.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp]
             L.fp8_amax_and_scale_update_ex.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp,
                                                        vp]
+            L.fp8_cast_transpose_pending.argtypes = [vp, i64, i64, vp, vp, vp, i32, i32, i32,
+                                                     i32, i32, i32, vp, vp, vp, i32, vp,
+                                                     c.c_uint, vp]
+            L.fp8_amax_and_scale_update_pending.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32,
+                                                            i32, i32, vp, vp]
             L.fp8_transpose.argtypes = [vp, i64, i64, vp, vp, vp]
             L.ct_device_error.argtypes = [c.POINTER(c.c_uint), i32]
             L.ct_selftest_bounded_wait.argtypes = [c.c_uint, vp]
@@ -97,6 +102,7 @@ def lib() -> ctypes.CDLL:
                          "fp8_dbias_cast_transpose", "fp8_dbias_cast_transpose_ex",
                          "fp8_multi_cast_transpose", "fp8_multi_cast_transpose_ex",
                          "fp8_amax_and_scale_update", "fp8_amax_and_scale_update_ex",
+                         "fp8_cast_transpose_pending", "fp8_amax_and_scale_update_pending",
                          "fp8_transpose", "ct_device_error"):
                 getattr(L, name).restype = i32
             _lib = L
@@ -257,6 +263,44 @@ def fp8_amax_and_scale_update_ex(amax_history, scale, scale_inv, fmt=E4M3, margi
         _dev(amax_history, "amax_history", torch.float32), _dev(scale, "scale", torch.float32, n),
         _dev(scale_inv, "scale_inv", torch.float32, n), L, n, fmt, margin, amax_algo,
         _opt(noop_flag, "noop_flag"), _stream(stream)))
+
+
+def fp8_cast_transpose_pending(x, amax_history, scale, pending, col, k, scale_inv, out, out_t,
+                               fmt=E4M3, margin=0, amax_algo=AMAX_MAX, noop_flag=None,
+                               stream=None, x_ready=False) -> None:
+    """Cast k of a run of casts on history column `col` whose scale updates
+    are deferred: the scale is derived from amax_history [L, n] and scale [n]
+    as they stood before the run and from pending rows 0 .. k-1 [K, n]; the
+    amax goes to pending[k, col]."""
+    rows, cols = _rc(x)
+    if amax_history.dim() != 2 or pending.dim() != 2:
+        raise ValueError("amax_history must be [hist_len, n] and pending [run, n]")
+    L, n = amax_history.shape
+    if pending.shape[1] != n or not 0 <= k < pending.shape[0]:
+        raise ValueError("pending must be [run, n] with k < run")
+    _check(lib().fp8_cast_transpose_pending(
+        _dev(x, "x", torch.bfloat16), rows, cols, _dev(amax_history, "amax_history", torch.float32),
+        _dev(scale, "scale", torch.float32, n), _dev(pending, "pending", torch.float32), L, n, col,
+        k, margin, amax_algo, _dev(scale_inv, "scale_inv", torch.float32, 1),
+        _dev(out, "out", _U8, rows * cols), _dev(out_t, "out_t", _U8, rows * cols), fmt,
+        _opt(noop_flag, "noop_flag"), X_READY if x_ready else 0, _stream(stream)))
+
+
+def fp8_amax_and_scale_update_pending(amax_history, scale, scale_inv, pending, fmt=E4M3,
+                                      margin=0, amax_algo=AMAX_MAX, noop_flag=None,
+                                      stream=None) -> None:
+    """The updates deferred by a run of len(pending) fp8_cast_transpose_pending
+    calls, applied at once; pending is zeroed."""
+    if amax_history.dim() != 2 or pending.dim() != 2:
+        raise ValueError("amax_history must be [hist_len, n] and pending [run, n]")
+    L, n = amax_history.shape
+    run = pending.shape[0]
+    if pending.shape[1] != n:
+        raise ValueError("pending must be [run, n]")
+    _check(lib().fp8_amax_and_scale_update_pending(
+        _dev(amax_history, "amax_history", torch.float32), _dev(scale, "scale", torch.float32, n),
+        _dev(scale_inv, "scale_inv", torch.float32, n), _dev(pending, "pending", torch.float32),
+        L, n, run, fmt, margin, amax_algo, _opt(noop_flag, "noop_flag"), _stream(stream)))
 
 
 def fp8_transpose(q, out_t, noop_flag=None, stream=None) -> None:

@@ -12,12 +12,17 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
 #include <vector>
 
 namespace {
+
+// Deferred updates: the longest history and run they take.
+constexpr int kPendingMaxHist = 1024;
+constexpr int kPendingMaxRun = 32;
 
 using ct::DirectParams;
 using ct::FastParams;
@@ -143,16 +148,18 @@ void fill_tensor(FastTensor& t, const void* out, const void* out_t, const float*
 // `runs_out` (dbias only): the number of partial rows the launched kernel
 // writes per column (one per band of tile rows on the TMA path, one per tile
 // row on the direct and general paths).  `x_ready`: CT_X_READY (TMA and
-// direct paths).
+// direct paths).  `pend`: deferred-update scale source (cast-transpose only:
+// the TMA kernel for every aligned shape, else the general kernel), or null
+// to cast with *scale.
 int cast_impl(const void* x, int64_t rows, int64_t cols, const float* scale, float* amax,
               float* scale_inv, void* out, void* out_t, float* partial, int fmt,
               const float* noop, cudaStream_t stream, int64_t* runs_out = nullptr,
-              bool x_ready = false) {
+              bool x_ready = false, const ct::PendingScale* pend = nullptr) {
     const int64_t R = (rows + ct::kTileRows - 1) / ct::kTileRows;
     const bool ragged_rows = ragged_rows_eligible(x, rows, cols, out, out_t);
     if (ragged_rows || fast_eligible(x, rows, cols, out, out_t)) {
         const int64_t tiles = R * ((cols + ct::kTileCols - 1) / ct::kTileCols);
-        if ((ragged_rows || tiles >= ct::kDirectMinTiles) && tiles <= INT32_MAX) {
+        if ((ragged_rows || tiles >= ct::kDirectMinTiles) && tiles <= INT32_MAX && !pend) {
             DirectParams<1> d;
             std::memset(&d, 0, sizeof(d));
             d.x[0] = static_cast<const uint16_t*>(x);
@@ -176,6 +183,7 @@ int cast_impl(const void* x, int64_t rows, int64_t cols, const float* scale, flo
         p.noop = noop;
         p.partial = partial;
         p.x_ready = x_ready ? 1 : 0;
+        if (pend) p.pend = *pend;
         if (runs_out) *runs_out = ct::dbias_units(R, R < ct::kDbiasBand ? R : ct::kDbiasBand).bands;
         return cuda_status(ct::launch_fast(p, fmt, partial != nullptr, out_t ? 0 : 1, stream));
     }
@@ -184,8 +192,8 @@ int cast_impl(const void* x, int64_t rows, int64_t cols, const float* scale, flo
     // flat cast followed by the FP8 transpose of q measured 2% faster than
     // the general kernel on 8191x12287 and 9% slower with cols % 8 == 4, so
     // cast-transpose stays on the general kernel.)
-    if (out_t == nullptr && partial == nullptr && out != nullptr && aligned(x, 16) &&
-        aligned(out, 8))
+    if (out_t == nullptr && partial == nullptr && pend == nullptr && out != nullptr &&
+        aligned(x, 16) && aligned(out, 8))
         return cuda_status(ct::launch_cast_flat(static_cast<const uint16_t*>(x), rows * cols,
                                                 static_cast<uint8_t*>(out), scale, amax, scale_inv,
                                                 fmt, noop, stream));
@@ -200,6 +208,7 @@ int cast_impl(const void* x, int64_t rows, int64_t cols, const float* scale, flo
     a.rows = rows;
     a.cols = cols;
     a.noop = noop;
+    a.pend = pend ? *pend : ct::PendingScale{};
     if (runs_out) *runs_out = R;
     return cuda_status(ct::launch_general(a, fmt, stream));
 }
@@ -443,6 +452,71 @@ int fp8_amax_and_scale_update(float* amax_history, float* scale, float* scale_in
                               const float* noop_flag, void* stream) {
     return fp8_amax_and_scale_update_ex(amax_history, scale, scale_inv, hist_len, n, fmt, margin,
                                         CT_AMAX_MAX, noop_flag, stream);
+}
+
+int fp8_cast_transpose_pending(const void* x, int64_t rows, int64_t cols,
+                               const float* amax_history, const float* scale, float* pending,
+                               int hist_len, int n, int col, int k, int margin, int amax_algo,
+                               float* scale_inv, void* out, void* out_t, int fmt,
+                               const float* noop_flag, unsigned flags, void* stream) {
+    if (flags & ~static_cast<unsigned>(CT_X_READY)) return CT_ERR_ARG;
+    if (hist_len < 1 || hist_len > kPendingMaxHist || n < 1 || col < 0 || col >= n || k < 0 ||
+        k >= kPendingMaxRun || k >= hist_len || margin < 0 || margin > 126)
+        return CT_ERR_ARG;
+    if (amax_algo != CT_AMAX_MAX && amax_algo != CT_AMAX_MOST_RECENT) return CT_ERR_ARG;
+    if (!amax_history || !scale || !pending) return CT_ERR_NULL;
+    if (!aligned(amax_history, 4) || !aligned(pending, 4)) return CT_ERR_ALIGN;
+    float* amax = pending + int64_t(k) * n + col;
+    const int st = check_cast(x, rows, cols, scale + col, amax, scale_inv, out, out_t, true, fmt);
+    if (st != CT_OK) return st;
+    if (rows == 0 || cols == 0) return CT_OK;
+    // the outputs against the inputs the scale is derived from
+    const Range rh = range_of(amax_history, int64_t(4) * hist_len * n);
+    const Range rs = range_of(scale, int64_t(4) * n), rp = range_of(pending, int64_t(4) * k * n);
+    const int64_t nq = rows * cols;
+    const Range outs[4] = {range_of(out, nq), range_of(out_t, nq), range_of(scale_inv, 4),
+                           range_of(amax, 4)};
+    for (const Range& o : outs)
+        if (overlap(o, rh) || overlap(o, rs) || overlap(o, rp)) return CT_ERR_ALIAS;
+    ct::PendingScale ps;
+    ps.hist = amax_history + col;
+    ps.scale0 = scale + col;
+    ps.pending = pending + col;
+    ps.stride = n;
+    ps.L = hist_len;
+    ps.k = k;
+    ps.most_recent = amax_algo == CT_AMAX_MOST_RECENT ? 1 : 0;
+    ps.fp8_max = fmt == CT_E4M3 ? 448.0f : 57344.0f;
+    ps.two_pow_margin = std::ldexp(1.0f, margin);
+    return cast_impl(x, rows, cols, scale + col, amax, scale_inv, out, out_t, nullptr, fmt,
+                     noop_flag, static_cast<cudaStream_t>(stream), nullptr,
+                     (flags & CT_X_READY) != 0, &ps);
+}
+
+int fp8_amax_and_scale_update_pending(float* amax_history, float* scale, float* scale_inv,
+                                      float* pending, int hist_len, int n, int run, int fmt,
+                                      int margin, int amax_algo, const float* noop_flag,
+                                      void* stream) {
+    if (n < 0 || hist_len < 1 || hist_len > kPendingMaxHist || run < 1 ||
+        run > kPendingMaxRun || run > hist_len || margin < 0 || margin > 126)
+        return CT_ERR_ARG;
+    if (amax_algo != CT_AMAX_MAX && amax_algo != CT_AMAX_MOST_RECENT) return CT_ERR_ARG;
+    if (fmt != CT_E4M3 && fmt != CT_E5M2) return CT_ERR_FORMAT;
+    if (n == 0) return CT_OK;
+    if (!amax_history || !scale || !scale_inv || !pending) return CT_ERR_NULL;
+    if (!aligned(amax_history, 4) || !aligned(scale, 4) || !aligned(scale_inv, 4) ||
+        !aligned(pending, 4))
+        return CT_ERR_ALIGN;
+    const Range rh = range_of(amax_history, int64_t(4) * hist_len * n);
+    const Range rs = range_of(scale, int64_t(4) * n), ri = range_of(scale_inv, int64_t(4) * n);
+    const Range rp = range_of(pending, int64_t(4) * run * n);
+    const Range all[4] = {rh, rs, ri, rp};
+    for (int i = 0; i < 4; ++i)
+        for (int j = i + 1; j < 4; ++j)
+            if (overlap(all[i], all[j])) return CT_ERR_ALIAS;
+    return cuda_status(ct::launch_scale_update_pending(
+        amax_history, pending, scale, scale_inv, hist_len, run, n, n, fmt, margin,
+        amax_algo == CT_AMAX_MOST_RECENT ? 1 : 0, noop_flag, static_cast<cudaStream_t>(stream)));
 }
 
 int fp8_transpose(const void* in, int64_t rows, int64_t cols, void* out, const float* noop_flag,

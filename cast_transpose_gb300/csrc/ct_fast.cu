@@ -37,6 +37,7 @@
 //     diagnostic bit, waits (bounded) for its own TMA loads and returns.
 #include "ct_device.cuh"
 #include "ct_internal.h"
+#include "ct_update.cuh"
 
 #include <mutex>
 
@@ -130,9 +131,12 @@ __device__ __forceinline__ void tile_coords(uint32_t local, uint32_t tile_rows, 
 // producer warp (warp kWarps) whose lane 0 drives the TMA pipeline.
 constexpr int kBlockThreads = kFastThreads + 32;
 
-template <int NT, int FMT, int STAGES, int MINB, bool WRITE_T, bool DBIAS>
+// PEND: a single tensor whose scale comes from deferred updates (p.pend);
+// the other instantiations are compiled without that code.
+template <int NT, int FMT, int STAGES, int MINB, bool WRITE_T, bool DBIAS, bool PEND = false>
 __global__ void __launch_bounds__(kBlockThreads, MINB)
     fast_cast_transpose_kernel(const __grid_constant__ FastParams<NT> p) {
+    static_assert(!PEND || (NT == 1 && WRITE_T && !DBIAS), "deferred updates: cast-transpose");
     using L = SmemLayout<STAGES, WRITE_T, DBIAS>;
     // Rows of the staged tile loaded per batch in pass 1: all at once for the
     // most loads in flight, 4 when registers are tight.
@@ -282,6 +286,10 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
     // flag, the scale, the amax slot): wait for it to complete first.
     dev::pdl_wait();
     if (p.noop != nullptr && *p.noop != 0.0f) return;
+    // single tensors with deferred updates: the scale, derived once per warp
+    // here, where every consumer warp is whole
+    float pend_scale = 0.0f;
+    if constexpr (PEND) pend_scale = dev::pending_scale_warp(p.pend, lane);
 
     // =============================== consumers ===============================
     int cur = -1;               // tensor of the current run, and its fields:
@@ -321,7 +329,7 @@ __global__ void __launch_bounds__(kBlockThreads, MINB)
             const StageInfo inf = info[s];
             if (inf.tensor != cur) {
                 cur = inf.tensor;
-                scale = *p.t[cur].scale;
+                scale = PEND ? pend_scale : *p.t[cur].scale;
                 rows = p.t[cur].rows;
                 cols = p.t[cur].cols;
                 out = p.t[cur].out;
@@ -507,10 +515,10 @@ int device_sms() {
     return sms;
 }
 
-template <int NT, int FMT, int STAGES, bool WRITE_T, bool DBIAS>
+template <int NT, int FMT, int STAGES, bool WRITE_T, bool DBIAS, bool PEND>
 cudaError_t launch_stages(const FastParams<NT>& p, int key, cudaStream_t stream) {
     using L = SmemLayout<STAGES, WRITE_T, DBIAS>;
-    auto kernel = fast_cast_transpose_kernel<NT, FMT, STAGES, kMinBlocks, WRITE_T, DBIAS>;
+    auto kernel = fast_cast_transpose_kernel<NT, FMT, STAGES, kMinBlocks, WRITE_T, DBIAS, PEND>;
     int sms = 0;
     cudaError_t e = prepare(kernel, key, L::bytes, &sms);
     if (e != cudaSuccess) return e;
@@ -520,12 +528,12 @@ cudaError_t launch_stages(const FastParams<NT>& p, int key, cudaStream_t stream)
                       stream, p);
 }
 
-template <int NT, int FMT, bool WRITE_T, bool DBIAS>
+template <int NT, int FMT, bool WRITE_T, bool DBIAS, bool PEND = false>
 cudaError_t launch_variant(const FastParams<NT>& p, int key, cudaStream_t stream) {
     const int64_t slots = int64_t(device_sms()) * kMinBlocks;
     if (slots > 0 && p.total_tiles > kLongRunTiles * slots)
-        return launch_stages<NT, FMT, kStagesLong, WRITE_T, DBIAS>(p, 2 * key + 1, stream);
-    return launch_stages<NT, FMT, kStagesShort, WRITE_T, DBIAS>(p, 2 * key, stream);
+        return launch_stages<NT, FMT, kStagesLong, WRITE_T, DBIAS, PEND>(p, 2 * key + 1, stream);
+    return launch_stages<NT, FMT, kStagesShort, WRITE_T, DBIAS, PEND>(p, 2 * key, stream);
 }
 
 }  // namespace
@@ -540,6 +548,9 @@ cudaError_t launch_fast(const FastParams<1>& p, int fmt, bool dbias, int variant
         return fmt == 0 ? launch_variant<1, 0, true, true>(p, 2, stream)
                         : launch_variant<1, 1, true, true>(p, 3, stream);
     }
+    if (p.pend.hist != nullptr)
+        return fmt == 0 ? launch_variant<1, 0, true, false, true>(p, 9, stream)
+                        : launch_variant<1, 1, true, false, true>(p, 10, stream);
     return fmt == 0 ? launch_variant<1, 0, true, false>(p, 4, stream)
                     : launch_variant<1, 1, true, false>(p, 5, stream);
 }

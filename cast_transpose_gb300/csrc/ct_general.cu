@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(256, DBIAS ? 3 : 4) general_cast_kernel(Genera
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c = tid & 15, rg = tid >> 4;
     const int b = lane & 7, w = warp * 4 + (lane >> 3);
-    const float scale = *a.scale;
+    const float scale = dev::cast_scale(a.scale, a.pend, lane);
 
     for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
         const int64_t rt = tile / tiles_c;
@@ -313,6 +313,25 @@ __global__ void __launch_bounds__(128) scale_update_long_kernel(float* __restric
     if (i >= n) return;
     dev::update_column_serial(hist + i, stride, L, scale + i, scale_inv + i, fp8_max,
                               two_pow_margin, most_recent);
+}
+
+// The K updates deferred by a run of casts (rule in ct_update.cuh), applied
+// at once: one warp per tensor.
+__global__ void __launch_bounds__(128) scale_update_pending_kernel(float* hist, float* pending,
+                                                                   float* scale, float* scale_inv,
+                                                                   int L, int K, int n,
+                                                                   int64_t stride, float fp8_max,
+                                                                   float two_pow_margin,
+                                                                   int most_recent,
+                                                                   const float* noop) {
+    dev::pdl_launch_dependents();
+    dev::pdl_wait();
+    if (noop != nullptr && *noop != 0.0f) return;
+    const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (i >= n) return;
+    const PendingScale ps{hist + i, scale + i, pending + i, stride, L, K, most_recent, fp8_max,
+                          two_pow_margin};
+    dev::apply_pending_warp(hist + i, pending + i, scale + i, scale_inv + i, ps, threadIdx.x & 31);
 }
 
 // ---------------------------------------------------------------------------
@@ -647,6 +666,18 @@ cudaError_t launch_scale_update(float* hist, float* scale, float* scale_inv, int
     const dim3 grid(static_cast<unsigned>((count + 127) / 128)), block(128);
     return launch_pdl(scale_update_long_kernel, grid, block, 0, stream, hist, scale, scale_inv,
                       hist_len, count, stride, fp8_max, two_pow_margin, most_recent, noop);
+}
+
+cudaError_t launch_scale_update_pending(float* hist, float* pending, float* scale,
+                                        float* scale_inv, int hist_len, int K, int count,
+                                        int64_t stride, int fmt, int margin, int most_recent,
+                                        const float* noop, cudaStream_t stream) {
+    const float fp8_max = fmt == 0 ? 448.0f : 57344.0f;
+    const float two_pow_margin = std::ldexp(1.0f, margin);   // exact for 0 <= margin <= 126
+    const dim3 grid(static_cast<unsigned>((int64_t(count) * 32 + 127) / 128)), block(128);
+    return launch_pdl(scale_update_pending_kernel, grid, block, 0, stream, hist, pending, scale,
+                      scale_inv, hist_len, K, count, stride, fp8_max, two_pow_margin, most_recent,
+                      noop);
 }
 
 cudaError_t launch_convert_f32(const float* in, int64_t n, int fmt, uint8_t* out,

@@ -21,6 +21,21 @@ constexpr unsigned kErrWaitTimeout = 1u;      // a kernel's mbarrier wait gave u
 constexpr unsigned kErrSelftestTimeout = 2u;  // the bounded-wait self-test gave up (expected)
 
 // One tensor of a TMA-path launch.  Pointers are device pointers.
+// Deferred scale updates (ct_update.cuh, "deferred updates"): a cast that
+// derives its scale from the history column as it stood before its run, the
+// scale then, and the amaxes of the run's earlier casts (pending rows).
+struct PendingScale {
+    const float* hist;     // history column before the run, row stride `stride` (null: none)
+    const float* scale0;   // the column's scale before the run
+    const float* pending;  // pending rows of the column, row stride `stride`
+    int64_t stride;
+    int L;                 // history length, 1 .. 1024
+    int k;                 // updates deferred so far, 0 .. min(32, L)
+    int most_recent;       // the "most recent" rule: a_j = c_j
+    float fp8_max;
+    float two_pow_margin;
+};
+
 struct FastTensor {
     uint8_t* out;          // [rows, cols] FP8 codes (may be null: not written)
     uint8_t* out_t;        // [cols, rows] FP8 codes (null when no transpose)
@@ -46,6 +61,7 @@ struct FastParams {
     float* partial;        // dbias partials [ceil(rows/128), cols], or null
     int x_ready;           // caller's promise: no kernel still running writes x
                            // (the first tiles may be loaded before the dependency wait)
+    PendingScale pend;     // single tensors: deferred-update scale (pend.hist null: t[0].scale)
 };
 
 // Arguments of the general (any shape / alignment) kernels.
@@ -60,6 +76,7 @@ struct GeneralArgs {
     int64_t rows;
     int64_t cols;
     const float* noop;
+    PendingScale pend;     // deferred-update scale (pend.hist null: *scale)
 };
 
 enum class Fmt : int { E4M3 = 0, E5M2 = 1 };
@@ -165,6 +182,12 @@ cudaError_t launch_dbias_finish(const float* partial, int64_t runs, int64_t cols
 cudaError_t launch_scale_update(float* hist, float* scale, float* scale_inv, int hist_len,
                                 int count, int64_t stride, int fmt, int margin, int most_recent,
                                 const float* noop, cudaStream_t stream);
+// The K deferred updates of `count` columns (hist_len <= 1024, 1 <= K <=
+// min(32, hist_len)); pending is [K, stride].
+cudaError_t launch_scale_update_pending(float* hist, float* pending, float* scale,
+                                        float* scale_inv, int hist_len, int K, int count,
+                                        int64_t stride, int fmt, int margin, int most_recent,
+                                        const float* noop, cudaStream_t stream);
 
 // FP8 byte transpose.  `fast` requires rows % 16 == 0, cols % 16 == 0 and
 // 16-byte aligned pointers.

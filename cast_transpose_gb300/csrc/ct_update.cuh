@@ -16,6 +16,8 @@
 // cast kernels' atomics.
 #pragma once
 
+#include "ct_internal.h"
+
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -108,6 +110,114 @@ __device__ __forceinline__ void update_column_serial(float* hist, int64_t stride
     finish_scale(a, __ldcg(scale), fp8_max, two_pow_margin, scale, scale_inv);
     for (int r = L - 1; r >= 1; --r) hist[int64_t(r) * stride] = __ldcg(hist + int64_t(r - 1) * stride);
     hist[0] = 0.0f;
+}
+
+// ---- deferred updates -------------------------------------------------------
+// A run of K casts that share history column i, each of which would be
+// followed by the update above, can defer the K updates to one pass after the
+// run.  Cast j of the run max-merges its amax into pending row j instead of
+// history row 0.  Write c_j for the amax that update j would have seen in
+// row 0: pending row j, and for j = 0 also history row 0 (the slot cast 0
+// would have merged into), merged the way the casts merge (the larger bit
+// pattern).  With H the history before the run, update j sees the window
+//   c_j, c_{j-1}, ..., c_0, H[1], ..., H[L-1-j]     (j < L),
+// so its maximum is the larger of max(c_0 .. c_j) and max(H[1 .. L-1-j]);
+// it replaces the scale by cand_j = (fp8_max / a_j) / 2^margin when the guard
+// passes and keeps the previous one otherwise.  The scale after k updates is
+// therefore cand_j of the latest j < k whose guard passes, or the scale before
+// the run when none does.  (Which NaN a window keeps does not matter: any
+// NaN fails the guard.)  The run's columns and positions: ct::PendingScale.
+
+// NaN-propagating maximum (identity: -inf).
+__device__ __forceinline__ float max_nan(float a, float b) {
+    return (isnan(a) || isnan(b)) ? __int_as_float(0x7FFFFFFF) : fmaxf(a, b);
+}
+
+// The scale after ps.k deferred updates, in every lane.  All 32 lanes of the
+// warp must call it.  Every load is issued before any result is used (one
+// round trip for histories of up to 32 + k rows): lane j holds c_j, lane i
+// history row L - k + i (the rows that leave the windows one per update),
+// and the lanes share the rows 1 .. L - k - 1 that every window keeps.
+__device__ __forceinline__ float pending_scale_warp(const PendingScale& ps, int lane) {
+    constexpr unsigned kAll = 0xFFFFFFFFu;
+    const int k = ps.k;
+    const float s0 = __ldcg(ps.scale0);
+    if (k == 0) return s0;
+    float c = -INFINITY, t = -INFINITY, h = -INFINITY;
+    const int m0 = ps.L - k;   // first row that leaves the window (update k - 1 sees rows 1 .. m0)
+    if (lane < k) {
+        c = __ldcg(ps.pending + int64_t(lane) * ps.stride);
+        if (lane == 0) c = __uint_as_float(max(__float_as_uint(c), __float_as_uint(__ldcg(ps.hist))));
+        if (m0 + lane >= 1) t = __ldcg(ps.hist + int64_t(m0 + lane) * ps.stride);
+    }
+#pragma unroll 8
+    for (int r = 1 + lane; r < m0; r += 32) h = max_nan(h, __ldcg(ps.hist + int64_t(r) * ps.stride));
+    const float c_own = c;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) h = max_nan(h, __shfl_xor_sync(kAll, h, off));
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {   // inclusive prefix maxima over the lanes
+        const float cu = __shfl_up_sync(kAll, c, off), tu = __shfl_up_sync(kAll, t, off);
+        if (lane >= off) {
+            c = max_nan(c, cu);
+            t = max_nan(t, tu);
+        }
+    }
+    // update j = lane: rows 1 .. L-1-j of H are the shared rows and tail rows 0 .. k-1-j
+    const float tj = __shfl_sync(kAll, t, (k - 1 - lane) & 31);
+    const float a = ps.most_recent ? c_own : max_nan(max_nan(c, h), tj);
+    float cand = 0.0f;
+    bool ok = false;
+    if (lane < k && a > 0.0f && isfinite(a)) {
+        cand = __fdiv_rn(__fdiv_rn(ps.fp8_max, a), ps.two_pow_margin);
+        ok = isfinite(cand);
+    }
+    const unsigned valid = __ballot_sync(kAll, ok);
+    if (valid == 0) return s0;
+    return __shfl_sync(kAll, cand, 31 - __clz(valid));
+}
+
+// The scale a cast kernel casts with: *scale, or the deferred-update scale
+// (uniform branch; with ps.hist set all 32 lanes must call it).
+__device__ __forceinline__ float cast_scale(const float* scale, const PendingScale& ps, int lane) {
+    return ps.hist != nullptr ? pending_scale_warp(ps, lane) : *scale;
+}
+
+// The K deferred updates of column i applied at once (one warp): scale and
+// scale_inv as after update K - 1, the window slid by K rows (row 0 := 0,
+// rows 1 .. K := c_{K-1} .. c_0, rows K+1 .. L-1 := H[1 .. L-1-K]) and the
+// pending rows cleared.  Every read happens before any write.
+__device__ __forceinline__ void apply_pending_warp(float* hist, float* pending, float* scale,
+                                                   float* scale_inv, const PendingScale& ps,
+                                                   int lane) {
+    const float s = pending_scale_warp(ps, lane);
+    const int K = ps.k, L = ps.L;
+    float c = 0.0f;
+    if (lane < K) {
+        c = __ldcg(pending + int64_t(lane) * ps.stride);
+        if (lane == 0) c = __uint_as_float(max(__float_as_uint(c), __float_as_uint(__ldcg(hist))));
+    }
+    float v[kUpdateRowsPerLane];
+#pragma unroll
+    for (int j = 0; j < kUpdateRowsPerLane; ++j) {
+        const int r = lane + 32 * j;   // row r of H moves to row r + K
+        v[j] = (r >= 1 && r + K < L) ? __ldcg(hist + int64_t(r) * ps.stride) : 0.0f;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < kUpdateRowsPerLane; ++j) {
+        const int r = lane + 32 * j;
+        if (r >= 1 && r + K < L) hist[int64_t(r + K) * ps.stride] = v[j];
+    }
+    if (lane < K) {
+        if (K - lane < L) hist[int64_t(K - lane) * ps.stride] = c;
+        pending[int64_t(lane) * ps.stride] = 0.0f;
+    }
+    if (lane == 0) {
+        hist[0] = 0.0f;
+        *scale = s;
+        *scale_inv = __fdiv_rn(1.0f, s);
+    }
 }
 
 }  // namespace dev

@@ -294,6 +294,80 @@ int fp8_amax_and_scale_update_ex(float* amax_history, float* scale, float* scale
                                  const float* noop_flag, void* stream);
 
 /*
+ * Deferred scale updates -- a run of casts that share one amax-history
+ * column, each of which would be followed by fp8_amax_and_scale_update_ex
+ * (the delayed-scaling update of [B], run after every refresh of a weight's
+ * FP8 copy).  The updates between the casts
+ * sit on the stream's critical path: each cast has to wait for the update
+ * before it.  Here cast k of the run instead derives the scale that the k
+ * updates before it would have produced, from the history and the scale as
+ * they stood before the run and from the amaxes of casts 0 .. k-1, and one
+ * fp8_amax_and_scale_update_pending call after the run applies all of them.
+ * Every cast's output and scale_inv, and the history, scale and scale_inv
+ * after the run, are bit for bit those of the sequence
+ *     for k in 0 .. K-1: fp8_cast_transpose_ex(x_k, ..., amax = history row 0
+ *                            of the column, ...);
+ *                        fp8_amax_and_scale_update_ex(...);
+ * (with the same hist_len, fmt, margin and amax_algo).
+ *
+ * fp8_cast_transpose_pending -- cast k (0-based) of such a run.
+ *
+ *   x, rows, cols, scale_inv, out, out_t, fmt, noop_flag, flags
+ *                 as fp8_cast_transpose_ex; scale_inv receives 1 / the derived
+ *                 scale
+ *   amax_history  fp32 [hist_len, n], read only: the history before the run
+ *   scale         fp32 [n], read only: the scales before the run
+ *   pending       fp32 [K, n] (K: the run's length), zero before cast 0 (and
+ *                 left zero by fp8_amax_and_scale_update_pending); rows 0 .. k-1
+ *                 are read (the amaxes of the earlier casts), row k is
+ *                 max-merged with max|x| (as `amax` of fp8_cast_transpose)
+ *   col           the history column, 0 <= col < n
+ *   k             0 <= k < min(32, hist_len)
+ *   hist_len, margin, amax_algo
+ *                 those of the deferred updates (fp8_amax_and_scale_update_ex);
+ *                 1 <= hist_len <= 1024; fp8_max is fmt's
+ *
+ * The scale: update j (0-based) sees the window c_j, c_{j-1}, .., c_0,
+ * history rows 1 .. hist_len-1-j, where c_j is pending row j (c_0 also
+ * max-merged with history row 0, the slot cast 0 would have merged into); the
+ * cast uses the guarded candidate (fp8_max / a_j) / 2^margin of the latest
+ * update j < k whose guard passes, else the scale before the run.  Every CTA
+ * derives it with one warp after the dependency wait, in the same round trip
+ * as the scale load it replaces.  The history, scale and pending rows 0 .. k-1
+ * must not be written by a kernel that may still be running when this call's
+ * kernel starts.  Outputs must not overlap x or each other, nor the history,
+ * the scale or pending rows 0 .. k-1.  Errors: as fp8_cast_transpose_ex, plus
+ * CT_ERR_ARG (hist_len, n, col, k, margin, amax_algo).
+ */
+int fp8_cast_transpose_pending(const void* x, int64_t rows, int64_t cols,
+                               const float* amax_history, const float* scale, float* pending,
+                               int hist_len, int n, int col, int k, int margin, int amax_algo,
+                               float* scale_inv, void* out, void* out_t, int fmt,
+                               const float* noop_flag, unsigned flags, void* stream);
+
+/*
+ * fp8_amax_and_scale_update_pending -- the `run` updates deferred by a run of
+ * fp8_cast_transpose_pending calls, applied to all n columns at once.
+ *
+ *   amax_history  fp32 [hist_len, n]: on return, as `run` calls of
+ *                 fp8_amax_and_scale_update_ex would leave it: row 0 = 0,
+ *                 rows 1 .. run = c_{run-1} .. c_0, the older rows slid down
+ *                 by `run`
+ *   scale, scale_inv  fp32 [n]: the scale after the last update, 1 / scale
+ *   pending       fp32 [run, n]: read, then set to 0
+ *   run           1 <= run <= min(32, hist_len);  1 <= hist_len <= 1024
+ *   fmt, margin, amax_algo, noop_flag  as fp8_amax_and_scale_update_ex
+ *
+ * One launch, one warp per column, every read before any write.  Buffers
+ * must not overlap.  Errors: CT_ERR_NULL, CT_ERR_ARG, CT_ERR_FORMAT,
+ * CT_ERR_ALIGN, CT_ERR_ALIAS, CT_ERR_CUDA.
+ */
+int fp8_amax_and_scale_update_pending(float* amax_history, float* scale, float* scale_inv,
+                                      float* pending, int hist_len, int n, int run, int fmt,
+                                      int margin, int amax_algo, const float* noop_flag,
+                                      void* stream);
+
+/*
  * fp8_transpose -- byte transpose of an existing FP8 tensor: the lazy
  * transpose-cache fill of [B] (transpose_2d(cache=True)), skippable through
  * the noop flag inside a captured graph.

@@ -215,3 +215,56 @@ def test_dbias_ex_x_ready_flag(L):
     assert ex(0x100 | 1, rows=0) == CT_OK          # empty: nothing launched
     assert ex(0x100, rows=0) == CT_OK
 
+
+
+def test_pending_cast_rejects(L):
+    H, P = DB, WS          # history and pending rows (fake addresses)
+
+    def cast(x=X, rows=64, cols=64, h=H, s=S, p=P, L_=16, n=2, col=1, k=3, margin=0, algo=0,
+             sinv=SI, q=Q, qt=QT, fmt=0, flags=0):
+        return L.fp8_cast_transpose_pending(x, rows, cols, h, s, p, L_, n, col, k, margin, algo,
+                                            sinv, q, qt, fmt, None, flags, None)
+    assert cast(flags=2) == CT_ERR_ARG
+    assert cast(L_=0) == CT_ERR_ARG
+    assert cast(L_=1025) == CT_ERR_ARG
+    assert cast(n=0) == CT_ERR_ARG
+    assert cast(col=2) == CT_ERR_ARG                   # col >= n
+    assert cast(col=-1) == CT_ERR_ARG
+    assert cast(k=-1) == CT_ERR_ARG
+    assert cast(k=16) == CT_ERR_ARG                    # k >= hist_len
+    assert cast(L_=64, k=32) == CT_ERR_ARG             # runs of at most 32 casts
+    assert cast(margin=127) == CT_ERR_ARG
+    assert cast(algo=2) == CT_ERR_ARG
+    assert cast(h=None) == CT_ERR_NULL
+    assert cast(p=None) == CT_ERR_NULL
+    assert cast(s=None) == CT_ERR_NULL
+    assert cast(x=None) == CT_ERR_NULL
+    assert cast(h=H + 2) == CT_ERR_ALIGN
+    assert cast(p=P + 2) == CT_ERR_ALIGN
+    assert cast(fmt=3) == CT_ERR_FORMAT
+    assert cast(sinv=H + 4) == CT_ERR_ALIAS            # scale_inv inside the history
+    assert cast(sinv=P) == CT_ERR_ALIAS                # scale_inv over pending row 0 (read)
+    assert cast(sinv=S + 4) == CT_ERR_ALIAS            # scale_inv over scale[1]
+    assert cast(qt=H) == CT_ERR_ALIAS
+    assert cast(rows=0) == CT_OK                       # empty: nothing launched
+
+
+def test_pending_update_rejects(L):
+    H, P = DB, WS
+
+    def upd(h=H, s=S, si=SI, p=P, L_=16, n=2, run=4, fmt=0, margin=0, algo=0):
+        return L.fp8_amax_and_scale_update_pending(h, s, si, p, L_, n, run, fmt, margin, algo,
+                                                   None, None)
+    assert upd(run=0) == CT_ERR_ARG
+    assert upd(run=17) == CT_ERR_ARG                   # run > hist_len
+    assert upd(L_=64, run=33) == CT_ERR_ARG
+    assert upd(L_=1025) == CT_ERR_ARG
+    assert upd(n=-1) == CT_ERR_ARG
+    assert upd(margin=-1) == CT_ERR_ARG
+    assert upd(algo=5) == CT_ERR_ARG
+    assert upd(fmt=2) == CT_ERR_FORMAT
+    assert upd(p=None) == CT_ERR_NULL
+    assert upd(p=P + 1) == CT_ERR_ALIGN
+    assert upd(si=S) == CT_ERR_ALIAS
+    assert upd(p=H + 8) == CT_ERR_ALIAS                # pending inside the history
+    assert upd(n=0) == CT_OK
