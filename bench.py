@@ -782,12 +782,16 @@ def secondary(dev, peaks, args) -> dict:
     res["cast_transpose 8191x12288 E4M3 (odd rows)"] = _rate_entry(
         ms, best, 4 * x.numel() + 12, peaks, "direct_cast_transpose_kernel (odd-row stores)")
     del x, q, qt
-    # ragged: odd rows and cols (the general kernel)
+    # ragged: odd rows and cols (the flat cast, then the FP8 transpose of q)
     x = workloads.normal_bf16(8191, 12287, 1.0, 17, dev)
     q, qt = ct.empty_outputs(x)
     ms, best = _timed(torch, lambda: ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3))
-    res["cast_transpose 8191x12287 E4M3 (ragged)"] = _rate_entry(ms, best, 4 * x.numel() + 12,
-                                                                 peaks, "general_cast_kernel")
+    res["cast_transpose 8191x12287 E4M3 (ragged)"] = _rate_entry(
+        ms, best, 4 * x.numel() + 12, peaks,
+        "cast_flat_kernel, then transpose_odd_kernel (q read back, mostly from L2)")
+    ms, best = _timed(torch, lambda: ct.fp8_transpose(q, qt))
+    res["transpose 8191x12287 FP8 (ragged)"] = _rate_entry(ms, best, 2 * x.numel(), peaks,
+                                                            "transpose_odd_kernel")
     ms, best = _timed(torch, lambda: ct.fp8_cast(x, s1, a0, si0, q, ct.E4M3))
     res["cast 8191x12287 E4M3 (ragged)"] = _rate_entry(ms, best, 3 * x.numel() + 12, peaks,
                                                        "cast_flat_kernel")
@@ -1035,8 +1039,12 @@ def profile_case(name: str) -> None:
       'list':       a 12-tensor list (the four list shapes at half size), then
                     three 48-column scale updates;
       'cast':       cast only of the activation, then three FP8 transposes;
-      'general':    cast-transpose of a ragged 8191x12287 matrix, then three
-                    FP8 transposes of its q (the general kernels);
+      'general':    cast-transpose of a ragged 8191x12287 matrix whose x
+                    starts 2 bytes past a 16-byte boundary (the general cast
+                    kernel);
+      'ragged':     cast-transpose of a ragged 8191x12287 matrix (the flat cast
+                    kernel, then the FP8 transpose of q), then three FP8
+                    transposes of q (the odd-shape transpose kernel);
       'flat':       three plain casts of the ragged 8191x12287 matrix (the flat
                     cast kernel);
       'odd':        cast-transpose of an 8191x12288 matrix (rows % 16 != 0:
@@ -1079,6 +1087,13 @@ def profile_case(name: str) -> None:
         for _ in range(3):
             ct.fp8_transpose(q, qt)
     elif name == "general":
+        buf = torch.empty(8191 * 12287 + 8, dtype=torch.bfloat16, device=dev)
+        x = buf[1:1 + 8191 * 12287].view(8191, 12287)
+        x.copy_(workloads.normal_bf16(8191, 12287, 1.0, 17, dev))
+        q, qt = ct.empty_outputs(x)
+        for _ in range(3):
+            ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3)
+    elif name == "ragged":
         x = workloads.normal_bf16(8191, 12287, 1.0, 17, dev)
         q, qt = ct.empty_outputs(x)
         for _ in range(3):
@@ -1138,7 +1153,8 @@ def _parse(argv=None):
     ap.add_argument("--extra", action=argparse.BooleanOptionalAction, default=True,
                     help="also time the secondary workloads")
     ap.add_argument("--profile-case",
-                    choices=["activation", "gradient", "list", "cast", "general", "flat", "odd",
+                    choices=["activation", "gradient", "list", "cast", "general", "ragged", "flat",
+                             "odd",
                              "loop", "noop", "weight"],
                     default=None,
                     help="only run 3 launches of one workload's kernel (for ncu) and exit")

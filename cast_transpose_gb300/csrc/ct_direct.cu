@@ -96,8 +96,8 @@ using dev::kColsumStride;
 // loads, four funnel shifts) and stores it with one 16-byte store.  The first
 // tile row owns [0, 128 - a_j) and the last [row0 - a_j, rows): their blocks
 // at the column ends are stored masked.
-constexpr int kHaloRows = 16;
-constexpr int kOddPitch = kHaloRows + kTileRows;
+constexpr int kHaloRows = gen::kHaloRows;
+constexpr int kOddPitch = gen::kColCopyPitch;
 
 // Word wd of halo row h (0 .. 15, copy row 128 + h) lives at wd ^ halo_swz(h):
 // the 8 lanes that read one word from rows 2b, 2b + 1 (b = 0 .. 7) then hit 8
@@ -130,54 +130,7 @@ __device__ __forceinline__ void odd_transpose_stores(const FastTensor& T, int64_
     }
     __syncwarp();
 
-    // a_j = (a0 + j * d) % 16 for column j of the tile
-    const int d = static_cast<int>(rows & 15);
-    const int a0 =
-        static_cast<int>((reinterpret_cast<uintptr_t>(T.out_t) + col0 * rows + row0) & 15);
-    const int k = lane & 7, g4 = lane >> 3;   // block k of column group g4
-    const bool last = row0 + kTileRows >= rows;
-    if (rt > 0 && !last) {
-        // The 4 columns of one store instruction lie sigma = 2^lsig apart,
-        // sigma such that their a_j differ by 4 (mod 16), so that their 4-byte
-        // loads fall in 4 distinct bank classes (d = 8 excepted: 2-way).
-        const int lsig = (d & 1) ? 2 : (d & 2) ? 1 : 0;
-        const int jb = 16 * warp + (g4 << lsig);
-        const int ab = a0 + jb * d;
-        uint8_t* const dst = T.out_t + (col0 + jb) * rows + row0 + 16 * k;
-        const uint8_t* const src = sqt + jb * kOddPitch + kHaloRows + 16 * k;
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int dj = ((it >> lsig) << (lsig + 2)) + (it & ((1 << lsig) - 1));
-            const int aj = (ab + dj * d) & 15;
-            const int s = dj * kOddPitch - aj;   // the block's first byte, from src
-            const uint32_t* p = reinterpret_cast<const uint32_t*>(src + (s & ~3));
-            const int sh = 8 * (s & 3);
-            const uint32_t w0 = p[0], w1 = p[1], w2 = p[2], w3 = p[3], w4 = p[4];
-            if (col0 + jb + dj < cols)
-                __stcs(reinterpret_cast<uint4*>(dst + dj * rows - aj),
-                       make_uint4(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh),
-                                  __funnelshift_r(w2, w3, sh), __funnelshift_r(w3, w4, sh)));
-        }
-    } else {   // first or last tile row: blocks 0 .. 8, cut to the rows the tile owns
-        const int L = static_cast<int>(last ? rows - row0 : kTileRows);
-        for (int e = lane; e < 16 * 9; e += 32) {
-            const int jq = e / 9, kk = e - 9 * jq, j = 16 * warp + jq;
-            if (col0 + j >= cols) continue;
-            const int aj = (a0 + j * d) & 15;
-            const int blk_row = 16 * kk - aj;   // tile row of the block's first byte
-            const int own_lo = rt > 0 ? -aj : 0, own_hi = last ? L : kTileRows - aj;
-            const int lo = max(0, own_lo - blk_row), hi = min(16, own_hi - blk_row);
-            if (lo >= hi) continue;
-            const int s = kHaloRows + blk_row;
-            const uint32_t* p = reinterpret_cast<const uint32_t*>(sqt + j * kOddPitch + (s & ~3));
-            const int sh = 8 * (s & 3);
-            const uint32_t v[4] = {__funnelshift_r(p[0], p[1], sh), __funnelshift_r(p[1], p[2], sh),
-                                   __funnelshift_r(p[2], p[3], sh), __funnelshift_r(p[3], p[4], sh)};
-            uint8_t* blk = T.out_t + (col0 + j) * rows + row0 + blk_row;
-            if (lo == 0 && hi == 16) __stcs(reinterpret_cast<uint4*>(blk), make_uint4(v[0], v[1], v[2], v[3]));
-            else gen::store_range(blk, v, lo, hi);
-        }
-    }
+    gen::store_col_copy_blocks(T.out_t, rows, cols, rt, row0, col0, sqt, lane, warp);
 }
 
 // EARLY: the launch issues work before the wait for the preceding kernel

@@ -6,6 +6,8 @@
 // stores when rows is not a multiple of 16.
 #pragma once
 
+#include "ct_internal.h"
+
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -219,6 +221,75 @@ __device__ __forceinline__ void store_segment_x8(uint8_t* seg, int L, const uint
                                    16 - m);
         const uint32_t t[4] = {t4.x, t4.y, t4.z, t4.w};
         store_tail(blk + 16, t, m);
+    }
+}
+
+// ---- whole aligned blocks of a tile's transpose ---------------------------
+// A 128x128 tile whose qT segments start at any byte (rows % 16 != 0, or a
+// misaligned out_t): column j's segment starts a_j = (out_t + col * rows +
+// row0) % 16 bytes into a 16-byte block.  An interior tile row owns the
+// rows [row0 - a_j, row0 + 128 - a_j) of column j, eight whole aligned
+// blocks, the first of which holds up to 15 rows of the tile above (its
+// halo); the first tile row owns [0, 128 - a_j) and the last [row0 - a_j,
+// rows), cut at the column ends.  The caller leaves the transpose in a
+// column-major copy: column j at j * kColCopyPitch, the 16 halo rows
+// (row0 - 16 .. row0 - 1) first, then the tile's rows.
+constexpr int kHaloRows = 16;
+constexpr int kColCopyPitch = kHaloRows + kTileRows;
+
+// Stores of the blocks of columns 16 * warp .. 16 * warp + 15 (one warp):
+// each block read back at its offset with five 4-byte loads and four funnel
+// shifts, then one 16-byte store; blocks cut at a column end are stored in
+// aligned pieces.  sqt needs 32 bytes of slack after the last column.
+__device__ __forceinline__ void store_col_copy_blocks(uint8_t* out_t, int64_t rows, int64_t cols,
+                                                      int64_t rt, int64_t row0, int64_t col0,
+                                                      const uint8_t* sqt, int lane, int warp) {
+    // a_j = (a0 + j * d) % 16 for column j of the tile
+    const int d = static_cast<int>(rows & 15);
+    const int a0 = static_cast<int>((reinterpret_cast<uintptr_t>(out_t) + col0 * rows + row0) & 15);
+    const int k = lane & 7, g4 = lane >> 3;   // block k of column group g4
+    const bool last = row0 + kTileRows >= rows;
+    if (rt > 0 && !last) {
+        // The 4 columns of one store instruction lie sigma = 2^lsig apart,
+        // sigma such that their a_j differ by 4 (mod 16), so that their 4-byte
+        // loads fall in 4 distinct bank classes (d = 0 or 8 excepted).
+        const int lsig = (d & 1) ? 2 : (d & 2) ? 1 : 0;
+        const int jb = 16 * warp + (g4 << lsig);
+        const int ab = a0 + jb * d;
+        uint8_t* const dst = out_t + (col0 + jb) * rows + row0 + 16 * k;
+        const uint8_t* const src = sqt + jb * kColCopyPitch + kHaloRows + 16 * k;
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int dj = ((it >> lsig) << (lsig + 2)) + (it & ((1 << lsig) - 1));
+            const int aj = (ab + dj * d) & 15;
+            const int s = dj * kColCopyPitch - aj;   // the block's first byte, from src
+            const uint32_t* p = reinterpret_cast<const uint32_t*>(src + (s & ~3));
+            const int sh = 8 * (s & 3);
+            const uint32_t w0 = p[0], w1 = p[1], w2 = p[2], w3 = p[3], w4 = p[4];
+            if (col0 + jb + dj < cols)
+                __stcs(reinterpret_cast<uint4*>(dst + dj * rows - aj),
+                       make_uint4(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh),
+                                  __funnelshift_r(w2, w3, sh), __funnelshift_r(w3, w4, sh)));
+        }
+    } else {   // first or last tile row: blocks 0 .. 8, cut to the rows the tile owns
+        const int L = static_cast<int>(last ? rows - row0 : kTileRows);
+        for (int e = lane; e < 16 * 9; e += 32) {
+            const int jq = e / 9, kk = e - 9 * jq, j = 16 * warp + jq;
+            if (col0 + j >= cols) continue;
+            const int aj = (a0 + j * d) & 15;
+            const int blk_row = 16 * kk - aj;   // tile row of the block's first byte
+            const int own_lo = rt > 0 ? -aj : 0, own_hi = last ? L : kTileRows - aj;
+            const int lo = max(0, own_lo - blk_row), hi = min(16, own_hi - blk_row);
+            if (lo >= hi) continue;
+            const int s = kHaloRows + blk_row;
+            const uint32_t* p = reinterpret_cast<const uint32_t*>(sqt + j * kColCopyPitch + (s & ~3));
+            const int sh = 8 * (s & 3);
+            const uint32_t v[4] = {__funnelshift_r(p[0], p[1], sh), __funnelshift_r(p[1], p[2], sh),
+                                   __funnelshift_r(p[2], p[3], sh), __funnelshift_r(p[3], p[4], sh)};
+            uint8_t* blk = out_t + (col0 + j) * rows + row0 + blk_row;
+            if (lo == 0 && hi == 16) __stcs(reinterpret_cast<uint4*>(blk), make_uint4(v[0], v[1], v[2], v[3]));
+            else store_range(blk, v, lo, hi);
+        }
     }
 }
 

@@ -417,6 +417,105 @@ __global__ void __launch_bounds__(256) transpose_fast_kernel(const uint8_t* __re
 // registers, else byte loads (first and last blocks of `in` only); bytes past
 // the row end are zeroed.  The transposed 16-byte blocks are stored with
 // gen::store_segment_x8 (aligned 16-byte blocks, masked at the segment ends).
+// FP8 transpose of any shape and alignment, one 128x128 tile per CTA.
+//   * Staging: row r of the tile is the byte segment in + g * cols + col0 of
+//     ncol bytes, starting e_r = its address % 16 into a 16-byte chunk.  The
+//     nine aligned chunks that cover it are copied as they are (cp.async, 16
+//     bytes each, no register round trip; nine consecutive lanes per row, so
+//     the copies of a warp are coalesced) into a 144-byte row of shared
+//     memory, together with the 16 rows of the tile above (the halo that the
+//     transposed stores below need).
+//   * Gather: warp b takes tile rows 16b .. 16b + 15, one row per load
+//     instruction: lane l reads the two aligned words that cover columns
+//     4l .. 4l + 3 of the row (at byte e_r + 4l) and funnel-shifts them, so a
+//     load touches 32 consecutive words (no bank conflict) and e_r is the same
+//     for the whole warp.  Since e_{r+1} = e_r + cols (mod 16), e_r depends on
+//     the row within the 16-row block only.  Byte permutes transpose each 4x4
+//     block; the column pieces go to a column-major copy (warp 0 also does the
+//     halo block).
+//   * Stores: gen::store_col_copy_blocks, whole aligned 16-byte blocks.
+constexpr int kOddStgRows = gen::kHaloRows + kTileRows;   // 144 staged rows
+constexpr int kOddStgPitch = 144;                         // 9 chunks of 16 bytes
+
+__global__ void __launch_bounds__(256) transpose_odd_kernel(const uint8_t* __restrict__ in,
+                                                            int64_t rows, int64_t cols,
+                                                            uint8_t* __restrict__ out,
+                                                            const float* noop) {
+    dev::pdl_launch_dependents();
+    dev::pdl_wait();
+    if (noop != nullptr && *noop != 0.0f) return;
+    __shared__ __align__(16) uint8_t stg[kOddStgRows * kOddStgPitch];
+    __shared__ __align__(16) uint8_t sqt[kTileCols * gen::kColCopyPitch + 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t tiles_c = static_cast<uint32_t>((cols + kTileCols - 1) / kTileCols);
+    const uint32_t rt32 = blockIdx.x / tiles_c;
+    const int64_t rt = rt32;
+    const int64_t row0 = rt * kTileRows;
+    const int64_t col0 = int64_t(blockIdx.x - rt32 * tiles_c) * kTileCols;
+    const int ncol = static_cast<int>(cols - col0 < kTileCols ? cols - col0 : kTileCols);
+    const uintptr_t ibeg = reinterpret_cast<uintptr_t>(in);
+    const uintptr_t iend = ibeg + uintptr_t(rows) * uintptr_t(cols);
+
+    // Staged row wr holds global row row0 - 16 + wr (rows before row 0 and
+    // from `rows` on are not loaded); chunk k of it at byte 16k.  Thread
+    // t < 252 copies chunk t % 9 of rows t / 9, t / 9 + 28, ...
+    if (tid < 252) {
+        const int k = tid % 9;
+        const int wr_lo = rt > 0 ? 0 : gen::kHaloRows;
+        const int64_t wr_hi64 = rows - row0 + gen::kHaloRows;
+        const int wr_hi = wr_hi64 < kOddStgRows ? static_cast<int>(wr_hi64) : kOddStgRows;
+        int wr = tid / 9;
+        uintptr_t a = ibeg + uintptr_t(row0 - gen::kHaloRows + wr) * uintptr_t(cols) + uintptr_t(col0);
+        const uintptr_t step = uintptr_t(28) * uintptr_t(cols);
+        for (; wr < kOddStgRows; wr += 28, a += step) {
+            if (wr < wr_lo || wr >= wr_hi) continue;
+            const int e = static_cast<int>(a & 15);
+            if (16 * k - e >= ncol) continue;   // the chunk starts past the row's segment
+            const uintptr_t c0 = (a & ~uintptr_t(15)) + 16 * uintptr_t(k);
+            uint8_t* dst = stg + wr * kOddStgPitch + 16 * k;
+            if (c0 >= ibeg) {
+                const uintptr_t n = iend - c0;   // > 0: the chunk holds a byte of the segment
+                dev::cp_async16(dst, reinterpret_cast<const void*>(c0), n < 16 ? static_cast<int>(n) : 16);
+            } else {   // the chunk that holds the first byte of `in`: only its bytes from there on
+                for (int i = static_cast<int>(ibeg - c0); i < 16 && c0 + i < iend; ++i)
+                    dst[i] = reinterpret_cast<const uint8_t*>(c0)[i];
+            }
+        }
+    }
+    dev::cp_async_wait_all();
+    __syncthreads();
+
+    // Row jj of every 16-row block starts e_jj = (E0 + jj * cols) % 16 bytes
+    // into its staged row (16 * cols = 0 mod 16), the same for every block.
+    const int cm = static_cast<int>(cols & 15);
+    const int E0 = static_cast<int>(
+        (ibeg + uintptr_t(row0 - gen::kHaloRows) * uintptr_t(cols) + uintptr_t(col0)) & 15);
+    auto block = [&](int wr0, int off) {   // staged rows wr0 .. wr0 + 15 -> column copy at `off`
+        const uint8_t* base = stg + wr0 * kOddStgPitch + 4 * lane;
+        uint32_t rw[16];
+        int e = E0;
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+            const uint32_t* w = reinterpret_cast<const uint32_t*>(base + jj * kOddStgPitch + (e & ~3));
+            rw[jj] = __funnelshift_r(w[0], w[1], 8 * (e & 3));
+            e = (e + cm) & 15;
+        }
+        uint32_t o[4][4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+            dev::transpose4x4(rw[4 * g], rw[4 * g + 1], rw[4 * g + 2], rw[4 * g + 3], o[0][g],
+                              o[1][g], o[2][g], o[3][g]);
+#pragma unroll
+        for (int kq = 0; kq < 4; ++kq)
+            *reinterpret_cast<uint4*>(sqt + (4 * lane + kq) * gen::kColCopyPitch + off) =
+                make_uint4(o[kq][0], o[kq][1], o[kq][2], o[kq][3]);
+    };
+    block(gen::kHaloRows + 16 * warp, gen::kHaloRows + 16 * warp);
+    if (warp == 0 && rt > 0) block(0, 0);
+    __syncthreads();
+    gen::store_col_copy_blocks(out, rows, cols, rt, row0, col0, sqt, lane, warp);
+}
+
 __global__ void __launch_bounds__(256) transpose_general_kernel(const uint8_t* __restrict__ in,
                                                                 int64_t rows, int64_t cols,
                                                                 uint8_t* __restrict__ out,
@@ -743,6 +842,9 @@ cudaError_t launch_transpose(const uint8_t* in, int64_t rows, int64_t cols, uint
                           0, stream, in, rows, cols, out, noop, loop_ctas, loop_tiles);
     }
     const int64_t tiles = ((rows + 127) / 128) * ((cols + 127) / 128);
+    if (tiles <= INT32_MAX)
+        return launch_pdl(transpose_odd_kernel, dim3(static_cast<unsigned>(tiles)), dim3(256), 0,
+                          stream, in, rows, cols, out, noop);
     return launch_pdl(transpose_general_kernel, dim3(grid_for(tiles, int64_t(1) << 30)), dim3(256), 0,
                       stream, in, rows, cols, out, noop);
 }
