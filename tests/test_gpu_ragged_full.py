@@ -1,0 +1,72 @@
+"""Full-size parity of the ragged shapes the benchmark times, each through the
+path it takes: every byte of q and qT against the oracle (rows split over
+spawned oracle processes on all host cores).
+
+  * 8191 x 12287 cast-transpose: the flat cast, then the odd-shape FP8
+    transpose of q;
+  * 8191 x 12288 cast-transpose: the direct kernel's odd-row variant (whole
+    aligned qT blocks with a halo from the tile above);
+  * 8191 x 12287 FP8 transpose of an existing q, and of a q that starts at an
+    odd byte, written to a qT at an odd byte.
+"""
+import numpy as np
+import pytest
+import torch
+
+import cast_transpose_gb300 as ct
+from cast_transpose_gb300 import workloads
+from gpu_util import Guarded, f32_bits, scalar
+from oracle_pool import OraclePool
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _no_device_error():
+    ct.device_error(clear=True)
+    yield
+    assert ct.device_error() == 0
+
+
+@pytest.mark.parametrize("shape,fmt", [((8191, 12287), ct.E4M3), ((8191, 12288), ct.E5M2)])
+def test_ragged_cast_transpose_in_full(shape, fmt):
+    rows, cols = shape
+    x = workloads.normal_bf16(rows, cols, 1.0, 17 + cols, "cuda")
+    n = rows * cols
+    q, qt = Guarded(n), Guarded(n)
+    s, a, si = scalar(1.75), scalar(0.0), scalar(-1.0)
+    ct.fp8_cast_transpose(x, s, a, si, q.t, qt.t, fmt)
+    torch.cuda.synchronize()
+    q.check()
+    qt.check()
+    with OraclePool() as pool:
+        xin = pool.input_bf16(rows, cols)
+        xin[:] = x.cpu().view(torch.int16).numpy().view(np.uint16)
+        qv = pool.output_q(rows, cols)
+        qv[:] = q.numpy().reshape(rows, cols)
+        qtv = pool.output_qt(rows, cols)
+        qtv[:] = qt.numpy().reshape(cols, rows)
+        res = pool.check_cast_transpose(rows, cols, 1.75, fmt, check_qt=True)
+        del xin, qv, qtv
+    assert res["bad_q"] == 0, ("FP8 data differs from the oracle", res["first_q"])
+    assert res["bad_qt"] == 0, ("transpose differs from the oracle", res["first_qt"])
+    assert f32_bits(a.item()) == f32_bits(res["amax"])
+    assert f32_bits(si.item()) == f32_bits(np.float32(1.0) / np.float32(1.75))
+
+
+@pytest.mark.parametrize("in_off,out_off", [(0, 0), (5, 11)])
+def test_odd_shape_fp8_transpose_in_full(in_off, out_off):
+    """The transpose is a byte permutation: qT must be exactly q's transpose."""
+    rows, cols = 8191, 12287
+    n = rows * cols
+    g = torch.Generator(device="cuda").manual_seed(23)
+    src = Guarded(n, offset=in_off)
+    src.t.copy_(torch.randint(0, 256, (n,), dtype=torch.int32, device="cuda", generator=g)
+                .to(torch.uint8))
+    dst = Guarded(n, offset=out_off)
+    ct.fp8_transpose(src.t.view(rows, cols), dst.t.view(cols, rows))
+    torch.cuda.synchronize()
+    src.check()
+    dst.check()
+    q = src.numpy().reshape(rows, cols)
+    assert np.array_equal(dst.numpy().reshape(cols, rows), q.T)
