@@ -15,6 +15,7 @@ import torch
 
 import cast_transpose_gb300 as ct
 from cast_transpose_gb300 import workloads
+import oracle
 from gpu_util import Guarded, f32_bits, scalar
 from oracle_pool import OraclePool
 
@@ -70,3 +71,29 @@ def test_odd_shape_fp8_transpose_in_full(in_off, out_off):
     dst.check()
     q = src.numpy().reshape(rows, cols)
     assert np.array_equal(dst.numpy().reshape(cols, rows), q.T)
+
+
+@pytest.mark.parametrize("shape", [(280, 250), (131, 255), (33, 127), (145, 383), (301, 263)])
+@pytest.mark.parametrize("x_shift,out_off", [(0, 10), (3, 0), (7, 15), (0, 1)])
+def test_ragged_kernel_row_ends(shape, x_shift, out_off):
+    """rows % 16 != 0 off the direct kernel's alignment (x off 16 bytes, or q
+    and qT at odd bytes; the general kernel, or the flat cast and the
+    odd-shape transpose), on shapes whose last column tile is nearly full:
+    every row end, at q offsets that put it anywhere in its 16-byte block."""
+    rows, cols = shape
+    x_cpu = workloads.normal_bf16(rows, cols, 3.0, rows * 7 + cols)
+    n = rows * cols
+    big = torch.empty(n + 16, dtype=torch.bfloat16, device="cuda")
+    big[x_shift:x_shift + n] = x_cpu.reshape(-1).cuda()
+    x = big[x_shift:x_shift + n].view(rows, cols)
+    q, qt = Guarded(n, offset=out_off), Guarded(n, offset=out_off)
+    s, a, si = scalar(0.625), scalar(0.0), scalar(-1.0)
+    ct.fp8_cast_transpose(x, s, a, si, q.t, qt.t, ct.E4M3)
+    torch.cuda.synchronize()
+    q.check()
+    qt.check()
+    ref = oracle.cast_transpose(x_cpu, 0.625, ct.E4M3)
+    assert np.array_equal(q.numpy().reshape(rows, cols), ref["q"])
+    assert np.array_equal(qt.numpy().reshape(cols, rows), ref["qt"])
+    assert f32_bits(a.item()) == f32_bits(ref["amax"])
+    assert f32_bits(si.item()) == f32_bits(ref["scale_inv"])
