@@ -516,91 +516,6 @@ __global__ void __launch_bounds__(256) transpose_odd_kernel(const uint8_t* __res
     gen::store_col_copy_blocks(out, rows, cols, rt, row0, col0, sqt, lane, warp);
 }
 
-__global__ void __launch_bounds__(256) transpose_general_kernel(const uint8_t* __restrict__ in,
-                                                                int64_t rows, int64_t cols,
-                                                                uint8_t* __restrict__ out,
-                                                                const float* noop) {
-    dev::pdl_launch_dependents();
-    dev::pdl_wait();
-    if (noop != nullptr && *noop != 0.0f) return;
-    __shared__ __align__(16) uint32_t tile[kTileRows * (kTileCols / 4)];
-    const int tid = threadIdx.x;
-    const int lane = tid & 31, warp = tid >> 5;
-    const uintptr_t ibeg = reinterpret_cast<uintptr_t>(in);
-    const uintptr_t iend = ibeg + uintptr_t(rows) * uintptr_t(cols);
-    const int64_t tiles_c = (cols + kTileCols - 1) / kTileCols;
-    const int64_t tiles = ((rows + kTileRows - 1) / kTileRows) * tiles_c;
-    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
-        const int64_t rt = t / tiles_c;
-        const int64_t row0 = rt * kTileRows, col0 = (t - rt * tiles_c) * kTileCols;
-        // chunk ch (16 bytes) of row r; 1024 chunks, 4 per thread
-        uint4 lo[4], hi[4];
-        int mode[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int idx = tid + 256 * i;
-            const int r = idx >> 3, ch = idx & 7;
-            const int64_t row = row0 + r, col = col0 + 16 * ch;
-            const int n = (row >= rows || col >= cols) ? 0
-                          : (cols - col >= 16 ? 16 : static_cast<int>(cols - col));
-            const uint8_t* src = in + row * cols + col;
-            const uintptr_t ad = reinterpret_cast<uintptr_t>(src);
-            const uintptr_t b0 = ad & ~uintptr_t(15);
-            lo[i] = make_uint4(0u, 0u, 0u, 0u);
-            hi[i] = lo[i];
-            mode[i] = 0;
-            if (n > 0) {
-                if (b0 == ad && b0 + 16 <= iend) {
-                    lo[i] = __ldg(reinterpret_cast<const uint4*>(b0));
-                    mode[i] = 1;
-                } else if (b0 >= ibeg && b0 + 32 <= iend) {
-                    lo[i] = __ldg(reinterpret_cast<const uint4*>(b0));
-                    hi[i] = __ldg(reinterpret_cast<const uint4*>(b0 + 16));
-                    mode[i] = 2;
-                } else {
-                    uint32_t e[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (j < n) e[j >> 2] |= uint32_t(__ldg(src + j)) << (8 * (j & 3));
-                    lo[i] = make_uint4(e[0], e[1], e[2], e[3]);
-                    mode[i] = 3;
-                }
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int idx = tid + 256 * i;
-            const int r = idx >> 3, ch = idx & 7;
-            const int64_t row = row0 + r, col = col0 + 16 * ch;
-            const int n = (row >= rows || col >= cols) ? 0
-                          : (cols - col >= 16 ? 16 : static_cast<int>(cols - col));
-            uint4 v = lo[i];
-            if (mode[i] == 2) {
-                const int m = static_cast<int>(reinterpret_cast<uintptr_t>(in + row * cols + col) & 15);
-                v = gen::extract16(lo[i], hi[i], m);
-            }
-            if (n < 16) v = gen::keep_first_bytes(v, n);
-            *reinterpret_cast<uint4*>(&tile[r * 32 + ((4 * ch) ^ (4 * (r >> 4)))]) = v;
-        }
-        __syncthreads();
-        const int b = lane & 7, w = warp * 4 + (lane >> 3);
-        uint32_t rw[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) rw[j] = tile[(16 * b + j) * 32 + (w ^ (4 * b))];
-        uint32_t o[4][4];
-#pragma unroll
-        for (int g = 0; g < 4; ++g)
-            dev::transpose4x4(rw[4 * g], rw[4 * g + 1], rw[4 * g + 2], rw[4 * g + 3], o[0][g],
-                              o[1][g], o[2][g], o[3][g]);
-        const int nrow = static_cast<int>(rows - row0 < kTileRows ? rows - row0 : kTileRows);
-#pragma unroll
-        for (int kq = 0; kq < 4; ++kq) {
-            const int64_t col = col0 + 4 * w + kq;
-            gen::store_segment_x8(out + col * rows + row0, col < cols ? nrow : 0, o[kq], b);
-        }
-        __syncthreads();
-    }
-}
 
 // ---------------------------------------------------------------------------
 // Flat cast: q[i] = fp8(x[i] * scale) over the n = rows * cols elements as
@@ -841,12 +756,11 @@ cudaError_t launch_transpose(const uint8_t* in, int64_t rows, int64_t cols, uint
         return launch_pdl(transpose_fast_kernel, dim3(grid_for(grid, int64_t(1) << 30)), dim3(256),
                           0, stream, in, rows, cols, out, noop, loop_ctas, loop_tiles);
     }
+    // at most 2^40 elements (the API's shape check): at most 2^26 tiles
     const int64_t tiles = ((rows + 127) / 128) * ((cols + 127) / 128);
-    if (tiles <= INT32_MAX)
-        return launch_pdl(transpose_odd_kernel, dim3(static_cast<unsigned>(tiles)), dim3(256), 0,
-                          stream, in, rows, cols, out, noop);
-    return launch_pdl(transpose_general_kernel, dim3(grid_for(tiles, int64_t(1) << 30)), dim3(256), 0,
-                      stream, in, rows, cols, out, noop);
+    if (tiles <= 0 || tiles > INT32_MAX) return cudaErrorInvalidValue;
+    return launch_pdl(transpose_odd_kernel, dim3(static_cast<unsigned>(tiles)), dim3(256), 0, stream,
+                      in, rows, cols, out, noop);
 }
 
 }  // namespace ct
