@@ -237,6 +237,34 @@ __device__ __forceinline__ void store_segment_x8(uint8_t* seg, int L, const uint
 constexpr int kHaloRows = 16;
 constexpr int kColCopyPitch = kHaloRows + kTileRows;
 
+// Interior tile rows: the 4 columns of one store instruction lie sigma =
+// 2^LSIG apart, sigma such that their a_j differ by 4 (mod 16), so that their
+// 4-byte loads fall in 4 distinct bank classes (d = 0 or 8 excepted).
+template <int LSIG>
+__device__ __forceinline__ void store_col_copy_interior(uint8_t* out_t, int64_t rows, int64_t cols,
+                                                        int64_t row0, int64_t col0, const uint8_t* sqt,
+                                                        int a0, int d, int k, int g4, int warp) {
+    const int jb = 16 * warp + (g4 << LSIG);
+    const int ab = a0 + jb * d;
+    const int64_t ncol_left = cols - col0 - jb;   // columns jb + dj < cols - col0 are stored
+    uint8_t* const dst = out_t + (col0 + jb) * rows + row0 + 16 * k;
+    const uint8_t* const src = sqt + jb * kColCopyPitch + kHaloRows + 16 * k;
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        constexpr int kMask = (1 << LSIG) - 1;
+        const int dj = ((it >> LSIG) << (LSIG + 2)) + (it & kMask);   // compile-time
+        const int aj = (ab + dj * d) & 15;
+        // the block's first byte: src + dj * pitch - aj (dj * pitch is a multiple of 4)
+        const uint32_t* p = reinterpret_cast<const uint32_t*>(src + dj * kColCopyPitch - ((aj + 3) & ~3));
+        const int sh = 8 * ((-aj) & 3);
+        const uint32_t w0 = p[0], w1 = p[1], w2 = p[2], w3 = p[3], w4 = p[4];
+        if (dj < ncol_left)
+            __stcs(reinterpret_cast<uint4*>(dst + dj * rows - aj),
+                   make_uint4(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh),
+                              __funnelshift_r(w2, w3, sh), __funnelshift_r(w3, w4, sh)));
+    }
+}
+
 // Stores of the blocks of columns 16 * warp .. 16 * warp + 15 (one warp):
 // each block read back at its offset with five 4-byte loads and four funnel
 // shifts, then one 16-byte store; blocks cut at a column end are stored in
@@ -250,27 +278,12 @@ __device__ __forceinline__ void store_col_copy_blocks(uint8_t* out_t, int64_t ro
     const int k = lane & 7, g4 = lane >> 3;   // block k of column group g4
     const bool last = row0 + kTileRows >= rows;
     if (rt > 0 && !last) {
-        // The 4 columns of one store instruction lie sigma = 2^lsig apart,
-        // sigma such that their a_j differ by 4 (mod 16), so that their 4-byte
-        // loads fall in 4 distinct bank classes (d = 0 or 8 excepted).
-        const int lsig = (d & 1) ? 2 : (d & 2) ? 1 : 0;
-        const int jb = 16 * warp + (g4 << lsig);
-        const int ab = a0 + jb * d;
-        uint8_t* const dst = out_t + (col0 + jb) * rows + row0 + 16 * k;
-        const uint8_t* const src = sqt + jb * kColCopyPitch + kHaloRows + 16 * k;
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int dj = ((it >> lsig) << (lsig + 2)) + (it & ((1 << lsig) - 1));
-            const int aj = (ab + dj * d) & 15;
-            const int s = dj * kColCopyPitch - aj;   // the block's first byte, from src
-            const uint32_t* p = reinterpret_cast<const uint32_t*>(src + (s & ~3));
-            const int sh = 8 * (s & 3);
-            const uint32_t w0 = p[0], w1 = p[1], w2 = p[2], w3 = p[3], w4 = p[4];
-            if (col0 + jb + dj < cols)
-                __stcs(reinterpret_cast<uint4*>(dst + dj * rows - aj),
-                       make_uint4(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh),
-                                  __funnelshift_r(w2, w3, sh), __funnelshift_r(w3, w4, sh)));
-        }
+        if (d & 1)
+            store_col_copy_interior<2>(out_t, rows, cols, row0, col0, sqt, a0, d, k, g4, warp);
+        else if (d & 2)
+            store_col_copy_interior<1>(out_t, rows, cols, row0, col0, sqt, a0, d, k, g4, warp);
+        else
+            store_col_copy_interior<0>(out_t, rows, cols, row0, col0, sqt, a0, d, k, g4, warp);
     } else {   // first or last tile row: blocks 0 .. 8, cut to the rows the tile owns
         const int L = static_cast<int>(last ? rows - row0 : kTileRows);
         for (int e = lane; e < 16 * 9; e += 32) {
