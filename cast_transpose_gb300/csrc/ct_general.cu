@@ -467,13 +467,23 @@ __global__ void __launch_bounds__(256) transpose_odd_kernel(const uint8_t* __res
         int wr = tid / 9;
         uintptr_t a = ibeg + uintptr_t(row0 - gen::kHaloRows + wr) * uintptr_t(cols) + uintptr_t(col0);
         const uintptr_t step = uintptr_t(28) * uintptr_t(cols);
+        // Unless the tile holds the first or the last 16-byte block of `in`,
+        // every chunk it copies lies within `in`: no per-chunk end checks.
+        const uintptr_t first =
+            ibeg + uintptr_t(row0 - gen::kHaloRows + wr_lo) * uintptr_t(cols) + uintptr_t(col0);
+        const uintptr_t last_end =
+            ibeg + uintptr_t(row0 - gen::kHaloRows + wr_hi - 1) * uintptr_t(cols) + uintptr_t(col0) +
+            uintptr_t(ncol);
+        const bool inside = (first & ~uintptr_t(15)) >= ibeg && ((last_end + 15) & ~uintptr_t(15)) <= iend;
         for (; wr < kOddStgRows; wr += 28, a += step) {
             if (wr < wr_lo || wr >= wr_hi) continue;
             const int e = static_cast<int>(a & 15);
             if (16 * k - e >= ncol) continue;   // the chunk starts past the row's segment
             const uintptr_t c0 = (a & ~uintptr_t(15)) + 16 * uintptr_t(k);
             uint8_t* dst = stg + wr * kOddStgPitch + 16 * k;
-            if (c0 >= ibeg) {
+            if (inside) {
+                dev::cp_async16(dst, reinterpret_cast<const void*>(c0), 16);
+            } else if (c0 >= ibeg) {
                 const uintptr_t n = iend - c0;   // > 0: the chunk holds a byte of the segment
                 dev::cp_async16(dst, reinterpret_cast<const void*>(c0), n < 16 ? static_cast<int>(n) : 16);
             } else {   // the chunk that holds the first byte of `in`: only its bytes from there on
