@@ -792,6 +792,16 @@ def secondary(dev, peaks, args) -> dict:
     ms, best = _timed(torch, lambda: ct.fp8_transpose(q, qt))
     res["transpose 8191x12287 FP8 (ragged)"] = _rate_entry(ms, best, 2 * x.numel(), peaks,
                                                             "transpose_odd_kernel")
+    flag = torch.zeros(1, device=dev)
+    ms, best = _timed(torch, lambda: ct.fp8_transpose(q, qt, noop_flag=flag))
+    res["transpose 8191x12287 FP8 (ragged), noop flag 0"] = _rate_entry(
+        ms, best, 2 * x.numel(), peaks,
+        "transpose_odd_kernel: a looping first wave over 90% of the tiles, then one tile per CTA")
+    flag.fill_(1.0)
+    ms, best = _timed(torch, lambda: ct.fp8_transpose(q, qt, noop_flag=flag), per_graph=50)
+    res["transpose 8191x12287 FP8 (ragged), noop flag 1"] = {
+        "us": round(ms * 1e3, 2), "us_best": round(best * 1e3, 2),
+        "note": "the same launch skipped by the flag"}
     ms, best = _timed(torch, lambda: ct.fp8_cast(x, s1, a0, si0, q, ct.E4M3))
     res["cast 8191x12287 E4M3 (ragged)"] = _rate_entry(ms, best, 3 * x.numel() + 12, peaks,
                                                        "cast_flat_kernel")

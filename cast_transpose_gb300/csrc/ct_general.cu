@@ -437,28 +437,22 @@ __global__ void __launch_bounds__(256) transpose_fast_kernel(const uint8_t* __re
 constexpr int kOddStgRows = gen::kHaloRows + kTileRows;   // 144 staged rows
 constexpr int kOddStgPitch = 144;                         // 9 chunks of 16 bytes
 
-__global__ void __launch_bounds__(256) transpose_odd_kernel(const uint8_t* __restrict__ in,
-                                                            int64_t rows, int64_t cols,
-                                                            uint8_t* __restrict__ out,
-                                                            const float* noop) {
-    dev::pdl_launch_dependents();
-    dev::pdl_wait();
-    if (noop != nullptr && *noop != 0.0f) return;
-    __shared__ __align__(16) uint8_t stg[kOddStgRows * kOddStgPitch];
-    __shared__ __align__(16) uint8_t sqt[kTileCols * gen::kColCopyPitch + 32];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint32_t tiles_c = static_cast<uint32_t>((cols + kTileCols - 1) / kTileCols);
-    const uint32_t rt32 = blockIdx.x / tiles_c;
+// One tile of the odd-shape transpose (the staging, gather and stores above).
+__device__ __forceinline__ void odd_transpose_tile(const uint8_t* __restrict__ in, int64_t rows,
+                                                   int64_t cols, uint8_t* __restrict__ out,
+                                                   uint32_t t, uint32_t tiles_c, uint8_t* stg,
+                                                   uint8_t* sqt, int tid, int lane, int warp) {
+    const uint32_t rt32 = t / tiles_c;
     const int64_t rt = rt32;
     const int64_t row0 = rt * kTileRows;
-    const int64_t col0 = int64_t(blockIdx.x - rt32 * tiles_c) * kTileCols;
+    const int64_t col0 = int64_t(t - rt32 * tiles_c) * kTileCols;
     const int ncol = static_cast<int>(cols - col0 < kTileCols ? cols - col0 : kTileCols);
     const uintptr_t ibeg = reinterpret_cast<uintptr_t>(in);
     const uintptr_t iend = ibeg + uintptr_t(rows) * uintptr_t(cols);
 
     // Staged row wr holds global row row0 - 16 + wr (rows before row 0 and
     // from `rows` on are not loaded); chunk k of it at byte 16k.  Thread
-    // t < 252 copies chunk t % 9 of rows t / 9, t / 9 + 28, ...
+    // i < 252 copies chunk i % 9 of rows i / 9, i / 9 + 28, ...
     if (tid < 252) {
         const int k = tid % 9;
         const int wr_lo = rt > 0 ? 0 : gen::kHaloRows;
@@ -524,6 +518,52 @@ __global__ void __launch_bounds__(256) transpose_odd_kernel(const uint8_t* __res
     if (warp == 0 && rt > 0) block(0, 0);
     __syncthreads();
     gen::store_col_copy_blocks(out, rows, cols, rt, row0, col0, sqt, lane, warp);
+}
+
+// One tile per CTA: calls without a noop flag.
+__global__ void __launch_bounds__(256) transpose_odd_kernel(const uint8_t* __restrict__ in,
+                                                            int64_t rows, int64_t cols,
+                                                            uint8_t* __restrict__ out,
+                                                            const float* noop) {
+    dev::pdl_launch_dependents();
+    dev::pdl_wait();
+    if (noop != nullptr && *noop != 0.0f) return;
+    __shared__ __align__(16) uint8_t stg[kOddStgRows * kOddStgPitch];
+    __shared__ __align__(16) uint8_t sqt[kTileCols * gen::kColCopyPitch + 32];
+    const int tid = threadIdx.x;
+    const uint32_t tiles_c = static_cast<uint32_t>((cols + kTileCols - 1) / kTileCols);
+    odd_transpose_tile(in, rows, cols, out, blockIdx.x, tiles_c, stg, sqt, tid, tid & 31, tid >> 5);
+}
+
+// Calls with a noop flag: the first loop_ctas CTAs (one wave) take tiles b,
+// b + loop_ctas, ... (loop_tiles each) and the CTAs after them one tile each
+// of the rest, so a launch that its flag skips starts few CTAs.  (The loop
+// costs the single-tile launch about 5%, so calls without a flag keep it.)
+__global__ void __launch_bounds__(256, 4) transpose_odd_loop_kernel(const uint8_t* __restrict__ in,
+                                                                    int64_t rows, int64_t cols,
+                                                                    uint8_t* __restrict__ out,
+                                                                    const float* noop,
+                                                                    int loop_ctas, int loop_tiles) {
+    dev::pdl_launch_dependents();
+    dev::pdl_wait();
+    if (noop != nullptr && *noop != 0.0f) return;
+    __shared__ __align__(16) uint8_t stg[kOddStgRows * kOddStgPitch];
+    __shared__ __align__(16) uint8_t sqt[kTileCols * gen::kColCopyPitch + 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t tiles_c = static_cast<uint32_t>((cols + kTileCols - 1) / kTileCols);
+    const uint32_t tiles = static_cast<uint32_t>((rows + kTileRows - 1) / kTileRows) * tiles_c;
+    uint32_t first = blockIdx.x, stride = 0, count = 1;
+    if (blockIdx.x < uint32_t(loop_ctas)) {
+        stride = loop_ctas;
+        count = loop_tiles;
+    } else {
+        first = uint32_t(loop_ctas) * uint32_t(loop_tiles) + (blockIdx.x - loop_ctas);
+    }
+    // A tile's gather ends before the barrier in front of its stores, so the
+    // next tile's staging never overwrites rows still being read.
+    uint32_t t = first;
+    for (uint32_t kt = 0; kt < count && t < tiles; ++kt, t += stride)
+        odd_transpose_tile(in, rows, cols, out, t, tiles_c, stg, sqt, tid, lane, warp);
 }
 
 
@@ -743,6 +783,25 @@ int transpose_wave_ctas() {
     return cache[dev];
 }
 
+// One wave of the odd-shape transpose's looping kernel: SMs x resident CTAs
+// (cached per device).
+int odd_transpose_wave_ctas() {
+    static std::mutex mu;
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        int sms = 0, per_sm = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, transpose_odd_loop_kernel, 256, 0) !=
+            cudaSuccess)
+            return 0;
+        cache[dev] = sms * per_sm;
+    }
+    return cache[dev];
+}
+
 cudaError_t launch_transpose(const uint8_t* in, int64_t rows, int64_t cols, uint8_t* out,
                              const float* noop, bool fast, cudaStream_t stream) {
     if (fast) {
@@ -766,9 +825,21 @@ cudaError_t launch_transpose(const uint8_t* in, int64_t rows, int64_t cols, uint
         return launch_pdl(transpose_fast_kernel, dim3(grid_for(grid, int64_t(1) << 30)), dim3(256),
                           0, stream, in, rows, cols, out, noop, loop_ctas, loop_tiles);
     }
-    // at most 2^40 elements (the API's shape check): at most 2^26 tiles
+    // at most 2^40 elements (the API's shape check): at most 2^26 tiles.
+    // With a noop flag, the same looping first wave as above.
     const int64_t tiles = ((rows + 127) / 128) * ((cols + 127) / 128);
     if (tiles <= 0 || tiles > INT32_MAX) return cudaErrorInvalidValue;
+    const int wave = noop != nullptr ? odd_transpose_wave_ctas() : 0;
+    if (wave > 0) {
+        const int64_t loop_ctas = wave;
+        int64_t loop_tiles = tiles * kTransposeLoopPercent / 100 / wave;
+        if (loop_tiles < 1) loop_tiles = 1;
+        const int64_t rest = tiles - loop_ctas * loop_tiles;
+        const int64_t grid = loop_ctas + (rest > 0 ? rest : 0);
+        return launch_pdl(transpose_odd_loop_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0,
+                          stream, in, rows, cols, out, noop, static_cast<int>(loop_ctas),
+                          static_cast<int>(loop_tiles));
+    }
     return launch_pdl(transpose_odd_kernel, dim3(static_cast<unsigned>(tiles)), dim3(256), 0, stream,
                       in, rows, cols, out, noop);
 }

@@ -73,12 +73,14 @@ def test_transpose_matches_oracle(shape):
     assert np.array_equal(out.numpy().reshape(cols, rows), oracle.fp8_transpose(q_cpu.numpy()))
 
 
-@pytest.mark.parametrize("shape", [(8192, 8192), (4112, 8208), (16, 4096)])
+@pytest.mark.parametrize("shape", [(8192, 8192), (4112, 8208), (16, 4096), (8191, 8193), (4111, 3001),
+                                   (17, 4095)])
 def test_transpose_with_noop_flag_zero(shape):
-    """With a noop flag (here 0) the aligned transpose runs a looping first
-    wave and one tile per CTA for the rest: 4096 tiles (several per looping
-    CTA), a partial last tile row and column (2145 tiles), and fewer tiles
-    than one wave."""
+    """With a noop flag (here 0) the transpose runs a looping first wave and
+    one tile per CTA for the rest: 4096 tiles (several per looping CTA), a
+    partial last tile row and column (2145 tiles), and fewer tiles than one
+    wave; the aligned kernel for the first three shapes, the odd-shape kernel
+    for the others."""
     rows, cols = shape
     g = torch.Generator().manual_seed(rows * 7 + cols)
     q_cpu = torch.randint(0, 256, (rows, cols), dtype=torch.uint8, generator=g)
@@ -87,6 +89,18 @@ def test_transpose_with_noop_flag_zero(shape):
     torch.cuda.synchronize()
     out.check()
     assert np.array_equal(out.numpy().reshape(cols, rows), oracle.fp8_transpose(q_cpu.numpy()))
+
+
+@pytest.mark.parametrize("shape", [(8192, 8192), (8191, 8193)])
+def test_transpose_with_noop_flag_set_writes_nothing(shape):
+    rows, cols = shape
+    q = torch.randint(0, 256, (rows, cols), dtype=torch.uint8, device="cuda")
+    out = Guarded(rows * cols)
+    out.t.fill_(0x5A)
+    ct.fp8_transpose(q, out.t, noop_flag=torch.ones(1, device="cuda"))
+    torch.cuda.synchronize()
+    out.check()
+    assert (out.numpy() == 0x5A).all()
 
 
 def test_transpose_misaligned():
