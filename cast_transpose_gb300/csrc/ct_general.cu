@@ -491,9 +491,17 @@ __device__ __forceinline__ void odd_transpose_tile(const uint8_t* __restrict__ i
 
     // Row jj of every 16-row block starts e_jj = (E0 + jj * cols) % 16 bytes
     // into its staged row (16 * cols = 0 mod 16), the same for every block.
+    // Lane l's four columns 4l .. 4l + 3 are taken rotated by rot = (l / 2) %
+    // 4 (byte c of its row word is column 4l + (c + rot) % 4), so that its
+    // k-th 16-byte column store goes to column 4l + (k + rot) % 4: the 8
+    // lanes of a store phase then hit 8 different 16-byte bank groups (with a
+    // 144-byte column pitch, columns 4l + k alone would share 2 of them).
     const int cm = static_cast<int>(cols & 15);
     const int E0 = static_cast<int>(
         (ibeg + uintptr_t(row0 - gen::kHaloRows) * uintptr_t(cols) + uintptr_t(col0)) & 15);
+    const int rot = (lane >> 1) & 3;
+    const uint32_t sel0 = 0x3210u + 0x1111u * rot - (rot > 0 ? 0x4000u : 0u) -
+                          (rot > 1 ? 0x0400u : 0u) - (rot > 2 ? 0x0040u : 0u);
     auto block = [&](int wr0, int off) {   // staged rows wr0 .. wr0 + 15 -> column copy at `off`
         const uint8_t* base = stg + wr0 * kOddStgPitch + 4 * lane;
         uint32_t rw[16];
@@ -501,7 +509,7 @@ __device__ __forceinline__ void odd_transpose_tile(const uint8_t* __restrict__ i
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
             const uint32_t* w = reinterpret_cast<const uint32_t*>(base + jj * kOddStgPitch + (e & ~3));
-            rw[jj] = __funnelshift_r(w[0], w[1], 8 * (e & 3));
+            rw[jj] = __byte_perm(w[0], w[1], sel0 + 0x1111u * static_cast<uint32_t>(e & 3));
             e = (e + cm) & 15;
         }
         uint32_t o[4][4];
@@ -509,9 +517,10 @@ __device__ __forceinline__ void odd_transpose_tile(const uint8_t* __restrict__ i
         for (int g = 0; g < 4; ++g)
             dev::transpose4x4(rw[4 * g], rw[4 * g + 1], rw[4 * g + 2], rw[4 * g + 3], o[0][g],
                               o[1][g], o[2][g], o[3][g]);
+        uint8_t* col = sqt + 4 * lane * gen::kColCopyPitch + off;
 #pragma unroll
         for (int kq = 0; kq < 4; ++kq)
-            *reinterpret_cast<uint4*>(sqt + (4 * lane + kq) * gen::kColCopyPitch + off) =
+            *reinterpret_cast<uint4*>(col + ((kq + rot) & 3) * gen::kColCopyPitch) =
                 make_uint4(o[kq][0], o[kq][1], o[kq][2], o[kq][3]);
     };
     block(gen::kHaloRows + 16 * warp, gen::kHaloRows + 16 * warp);
