@@ -427,12 +427,13 @@ __global__ void __launch_bounds__(256) transpose_fast_kernel(const uint8_t* __re
 //     transposed stores below need).
 //   * Gather: warp b takes tile rows 16b .. 16b + 15, one row per load
 //     instruction: lane l reads the two aligned words that cover columns
-//     4l .. 4l + 3 of the row (at byte e_r + 4l) and funnel-shifts them, so a
-//     load touches 32 consecutive words (no bank conflict) and e_r is the same
-//     for the whole warp.  Since e_{r+1} = e_r + cols (mod 16), e_r depends on
-//     the row within the 16-row block only.  Byte permutes transpose each 4x4
-//     block; the column pieces go to a column-major copy (warp 0 also does the
-//     halo block).
+//     4l .. 4l + 3 of the row (at byte e_r + 4l) and byte-permutes them into
+//     one word, so a load touches 32 consecutive words (no bank conflict) and
+//     e_r is the same for the whole warp.  Since e_{r+1} = e_r + cols (mod
+//     16), e_r depends on the row within the 16-row block only.  Byte
+//     permutes transpose each 4x4 block; the column pieces go to a
+//     column-major copy.  Warps 0 .. 3 also take 4 halo rows each (warp 0
+//     taking all 16 left the other seven waiting for it at the barrier).
 //   * Stores: gen::store_col_copy_blocks, whole aligned 16-byte blocks.
 constexpr int kOddStgRows = gen::kHaloRows + kTileRows;   // 144 staged rows
 constexpr int kOddStgPitch = 144;                         // 9 chunks of 16 bytes
@@ -524,7 +525,23 @@ __device__ __forceinline__ void odd_transpose_tile(const uint8_t* __restrict__ i
                 make_uint4(o[kq][0], o[kq][1], o[kq][2], o[kq][3]);
     };
     block(gen::kHaloRows + 16 * warp, gen::kHaloRows + 16 * warp);
-    if (warp == 0 && rt > 0) block(0, 0);
+    if (rt > 0 && warp < 4) {   // halo rows 4 warp .. 4 warp + 3: one 4x4 block per lane
+        const uint8_t* base = stg + 4 * warp * kOddStgPitch + 4 * lane;
+        uint32_t rw[4];
+        int e = (E0 + 4 * warp * cm) & 15;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const uint32_t* w = reinterpret_cast<const uint32_t*>(base + jj * kOddStgPitch + (e & ~3));
+            rw[jj] = __byte_perm(w[0], w[1], sel0 + 0x1111u * static_cast<uint32_t>(e & 3));
+            e = (e + cm) & 15;
+        }
+        uint32_t c[4];
+        dev::transpose4x4(rw[0], rw[1], rw[2], rw[3], c[0], c[1], c[2], c[3]);
+        uint8_t* col = sqt + 4 * lane * gen::kColCopyPitch + 4 * warp;
+#pragma unroll
+        for (int kq = 0; kq < 4; ++kq)
+            *reinterpret_cast<uint32_t*>(col + ((kq + rot) & 3) * gen::kColCopyPitch) = c[kq];
+    }
     __syncthreads();
     gen::store_col_copy_blocks(out, rows, cols, rt, row0, col0, sqt, lane, warp);
 }
@@ -812,7 +829,7 @@ int odd_transpose_wave_ctas() {
 }
 
 cudaError_t launch_transpose(const uint8_t* in, int64_t rows, int64_t cols, uint8_t* out,
-                             const float* noop, bool fast, cudaStream_t stream) {
+                             const float* noop, bool fast, cudaStream_t stream, bool after_cast) {
     if (fast) {
         const int64_t tiles = ((rows + 127) / 128) * ((cols + 127) / 128);
         // Without a noop flag, one tile per CTA: the hardware hands tiles to
@@ -835,10 +852,14 @@ cudaError_t launch_transpose(const uint8_t* in, int64_t rows, int64_t cols, uint
                           0, stream, in, rows, cols, out, noop, loop_ctas, loop_tiles);
     }
     // at most 2^40 elements (the API's shape check): at most 2^26 tiles.
-    // With a noop flag, the same looping first wave as above.
+    // With a noop flag, the same looping first wave as above.  So too right
+    // after the flat cast: there the one-tile kernel (48 registers, 5 CTAs
+    // per SM) loses to the looping one (4 CTAs per SM), though alone it wins;
+    // 8191x12287 measured: cast + transpose 4.15 against 4.51 TB/s,
+    // transpose alone 42.1 against 44.7 us.
     const int64_t tiles = ((rows + 127) / 128) * ((cols + 127) / 128);
     if (tiles <= 0 || tiles > INT32_MAX) return cudaErrorInvalidValue;
-    const int wave = noop != nullptr ? odd_transpose_wave_ctas() : 0;
+    const int wave = noop != nullptr || after_cast ? odd_transpose_wave_ctas() : 0;
     if (wave > 0) {
         const int64_t loop_ctas = wave;
         int64_t loop_tiles = tiles * kTransposeLoopPercent / 100 / wave;

@@ -190,9 +190,11 @@ cudaError_t launch_scale_update_pending(float* hist, float* pending, float* scal
                                         const float* noop, cudaStream_t stream);
 
 // FP8 byte transpose.  `fast` requires rows % 16 == 0, cols % 16 == 0 and
-// 16-byte aligned pointers.
+// 16-byte aligned pointers.  `after_cast`: the transpose of a q that the flat
+// cast has just written (the odd-shape kernel then takes the looping launch).
 cudaError_t launch_transpose(const uint8_t* in, int64_t rows, int64_t cols, uint8_t* out,
-                             const float* noop, bool fast, cudaStream_t stream);
+                             const float* noop, bool fast, cudaStream_t stream,
+                             bool after_cast = false);
 
 // FP8 conversion of n fp32 values (no scale): the cast kernels' conversion step.
 cudaError_t launch_convert_f32(const float* in, int64_t n, int fmt, uint8_t* out,
