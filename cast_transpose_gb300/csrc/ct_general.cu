@@ -435,6 +435,9 @@ __global__ void __launch_bounds__(256) transpose_fast_kernel(const uint8_t* __re
 //     column-major copy.  Warps 0 .. 3 also take 4 halo rows each (warp 0
 //     taking all 16 left the other seven waiting for it at the barrier).
 //   * Stores: gen::store_col_copy_blocks, whole aligned 16-byte blocks.
+#ifndef V_REV
+#define V_REV 1
+#endif
 constexpr int kOddStgRows = gen::kHaloRows + kTileRows;   // 144 staged rows
 constexpr int kOddStgPitch = 144;                         // 9 chunks of 16 bytes
 
@@ -569,7 +572,8 @@ __global__ void __launch_bounds__(256, 4) transpose_odd_loop_kernel(const uint8_
                                                                     int64_t rows, int64_t cols,
                                                                     uint8_t* __restrict__ out,
                                                                     const float* noop,
-                                                                    int loop_ctas, int loop_tiles) {
+                                                                    int loop_ctas, int loop_tiles,
+                                                                    int reverse) {
     dev::pdl_launch_dependents();
     dev::pdl_wait();
     if (noop != nullptr && *noop != 0.0f) return;
@@ -589,7 +593,8 @@ __global__ void __launch_bounds__(256, 4) transpose_odd_loop_kernel(const uint8_
     // next tile's staging never overwrites rows still being read.
     uint32_t t = first;
     for (uint32_t kt = 0; kt < count && t < tiles; ++kt, t += stride)
-        odd_transpose_tile(in, rows, cols, out, t, tiles_c, stg, sqt, tid, lane, warp);
+        odd_transpose_tile(in, rows, cols, out, reverse ? tiles - 1 - t : t, tiles_c, stg, sqt, tid,
+                           lane, warp);
 }
 
 
@@ -868,7 +873,7 @@ cudaError_t launch_transpose(const uint8_t* in, int64_t rows, int64_t cols, uint
         const int64_t grid = loop_ctas + (rest > 0 ? rest : 0);
         return launch_pdl(transpose_odd_loop_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0,
                           stream, in, rows, cols, out, noop, static_cast<int>(loop_ctas),
-                          static_cast<int>(loop_tiles));
+                          static_cast<int>(loop_tiles), after_cast && V_REV ? 1 : 0);
     }
     return launch_pdl(transpose_odd_kernel, dim3(static_cast<unsigned>(tiles)), dim3(256), 0, stream,
                       in, rows, cols, out, noop);
