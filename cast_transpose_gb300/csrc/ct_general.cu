@@ -435,9 +435,6 @@ __global__ void __launch_bounds__(256) transpose_fast_kernel(const uint8_t* __re
 //     column-major copy.  Warps 0 .. 3 also take 4 halo rows each (warp 0
 //     taking all 16 left the other seven waiting for it at the barrier).
 //   * Stores: gen::store_col_copy_blocks, whole aligned 16-byte blocks.
-#ifndef V_REV
-#define V_REV 1
-#endif
 constexpr int kOddStgRows = gen::kHaloRows + kTileRows;   // 144 staged rows
 constexpr int kOddStgPitch = 144;                         // 9 chunks of 16 bytes
 
@@ -564,10 +561,12 @@ __global__ void __launch_bounds__(256) transpose_odd_kernel(const uint8_t* __res
     odd_transpose_tile(in, rows, cols, out, blockIdx.x, tiles_c, stg, sqt, tid, tid & 31, tid >> 5);
 }
 
-// Calls with a noop flag: the first loop_ctas CTAs (one wave) take tiles b,
-// b + loop_ctas, ... (loop_tiles each) and the CTAs after them one tile each
-// of the rest, so a launch that its flag skips starts few CTAs.  (The loop
-// costs the single-tile launch about 5%, so calls without a flag keep it.)
+// Calls with a noop flag, and the transpose right after the flat cast: the
+// first loop_ctas CTAs (one wave) take tiles b, b + loop_ctas, ...
+// (loop_tiles each) and the CTAs after them one tile each of the rest, so a
+// launch that its flag skips starts few CTAs.  `reverse` takes the tiles
+// from the last one back: after the flat cast, whose last rows of q are the
+// ones still in L2.
 __global__ void __launch_bounds__(256, 4) transpose_odd_loop_kernel(const uint8_t* __restrict__ in,
                                                                     int64_t rows, int64_t cols,
                                                                     uint8_t* __restrict__ out,
@@ -861,7 +860,8 @@ cudaError_t launch_transpose(const uint8_t* in, int64_t rows, int64_t cols, uint
     // after the flat cast: there the one-tile kernel (48 registers, 5 CTAs
     // per SM) loses to the looping one (4 CTAs per SM), though alone it wins;
     // 8191x12287 measured: cast + transpose 4.15 against 4.51 TB/s,
-    // transpose alone 42.1 against 44.7 us.
+    // transpose alone 42.1 against 44.7 us.  After the cast the looping
+    // launch also takes the tiles in reverse order (4.51 -> 4.59 TB/s).
     const int64_t tiles = ((rows + 127) / 128) * ((cols + 127) / 128);
     if (tiles <= 0 || tiles > INT32_MAX) return cudaErrorInvalidValue;
     const int wave = noop != nullptr || after_cast ? odd_transpose_wave_ctas() : 0;
@@ -873,7 +873,7 @@ cudaError_t launch_transpose(const uint8_t* in, int64_t rows, int64_t cols, uint
         const int64_t grid = loop_ctas + (rest > 0 ? rest : 0);
         return launch_pdl(transpose_odd_loop_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0,
                           stream, in, rows, cols, out, noop, static_cast<int>(loop_ctas),
-                          static_cast<int>(loop_tiles), after_cast && V_REV ? 1 : 0);
+                          static_cast<int>(loop_tiles), after_cast ? 1 : 0);
     }
     return launch_pdl(transpose_odd_kernel, dim3(static_cast<unsigned>(tiles)), dim3(256), 0, stream,
                       in, rows, cols, out, noop);
