@@ -197,7 +197,8 @@ int cast_impl(const void* x, int64_t rows, int64_t cols, const float* scale, flo
         aligned(out, 8) && (out_t == nullptr || rows % 16 != 0)) {
         const cudaError_t e = ct::launch_cast_flat(static_cast<const uint16_t*>(x), rows * cols,
                                                    static_cast<uint8_t*>(out), scale, amax,
-                                                   scale_inv, fmt, noop, stream);
+                                                   scale_inv, fmt, noop, stream,
+                                                   /*keep_q=*/out_t != nullptr);
         if (e != cudaSuccess || out_t == nullptr) return cuda_status(e);
         const bool tfast = rows % 16 == 0 && cols % 16 == 0 && aligned(out, 16) &&
                            aligned(out_t, 16);

@@ -442,7 +442,8 @@ constexpr int kOddStgPitch = 144;                         // 9 chunks of 16 byte
 __device__ __forceinline__ void odd_transpose_tile(const uint8_t* __restrict__ in, int64_t rows,
                                                    int64_t cols, uint8_t* __restrict__ out,
                                                    uint32_t t, uint32_t tiles_c, uint8_t* stg,
-                                                   uint8_t* sqt, int tid, int lane, int warp) {
+                                                   uint8_t* sqt, int tid, int lane, int warp,
+                                                   bool demote = false) {
     const uint32_t rt32 = t / tiles_c;
     const int64_t rt = rt32;
     const int64_t row0 = rt * kTileRows;
@@ -489,6 +490,15 @@ __device__ __forceinline__ void odd_transpose_tile(const uint8_t* __restrict__ i
     }
     dev::cp_async_wait_all();
     __syncthreads();
+    if (demote) {   // the tile's own q rows, now staged, back to the normal L2 priority
+        const int64_t g = row0 + (tid >> 1);
+        if (g < rows) {   // the one or two 128-byte lines of row g's segment
+            const uintptr_t a = ibeg + uintptr_t(g) * uintptr_t(cols) + uintptr_t(col0);
+            const uintptr_t line = (a & ~uintptr_t(127)) + 128 * uintptr_t(tid & 1);
+            if (line < a + uintptr_t(ncol))
+                asm volatile("applypriority.global.L2::evict_normal [%0], 128;" ::"l"(line) : "memory");
+        }
+    }
 
     // Row jj of every 16-row block starts e_jj = (E0 + jj * cols) % 16 bytes
     // into its staged row (16 * cols = 0 mod 16), the same for every block.
@@ -564,9 +574,10 @@ __global__ void __launch_bounds__(256) transpose_odd_kernel(const uint8_t* __res
 // Calls with a noop flag, and the transpose right after the flat cast: the
 // first loop_ctas CTAs (one wave) take tiles b, b + loop_ctas, ...
 // (loop_tiles each) and the CTAs after them one tile each of the rest, so a
-// launch that its flag skips starts few CTAs.  `reverse` takes the tiles
-// from the last one back: after the flat cast, whose last rows of q are the
-// ones still in L2.
+// launch that its flag skips starts few CTAs.  `reverse` (after the flat
+// cast) takes the tiles from the last one back, since the last rows of q are
+// the ones still in L2, and returns the lines of q that the cast stored with
+// the evict-last priority to the normal one once a tile has staged them.
 __global__ void __launch_bounds__(256, 4) transpose_odd_loop_kernel(const uint8_t* __restrict__ in,
                                                                     int64_t rows, int64_t cols,
                                                                     uint8_t* __restrict__ out,
@@ -593,7 +604,7 @@ __global__ void __launch_bounds__(256, 4) transpose_odd_loop_kernel(const uint8_
     uint32_t t = first;
     for (uint32_t kt = 0; kt < count && t < tiles; ++kt, t += stride)
         odd_transpose_tile(in, rows, cols, out, reverse ? tiles - 1 - t : t, tiles_c, stg, sqt, tid,
-                           lane, warp);
+                           lane, warp, reverse != 0);
 }
 
 
@@ -609,7 +620,22 @@ __global__ void __launch_bounds__(256, 4) transpose_odd_loop_kernel(const uint8_
 constexpr int kFlatPerThread = 8;
 constexpr int64_t kFlatChunks = 256 * kFlatPerThread;
 
-template <int FMT>
+// The 8-byte store of a flat-cast chunk; KEEP: with the L2 evict-last
+// priority (the transpose that reads q next lowers it again).
+template <bool KEEP>
+__device__ __forceinline__ void store_q8(uint2* p, uint2 v) {
+    if (KEEP) {
+        uint64_t pol;
+        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+        asm volatile("st.global.L2::cache_hint.v2.u32 [%0], {%1, %2}, %3;" ::"l"(p), "r"(v.x),
+                     "r"(v.y), "l"(pol)
+                     : "memory");
+    } else {
+        *p = v;
+    }
+}
+
+template <int FMT, bool KEEP>
 __global__ void __launch_bounds__(256) cast_flat_kernel(const uint16_t* __restrict__ x, int64_t n,
                                                         uint8_t* __restrict__ q, const float* scale_p,
                                                         float* amax, float* scale_inv,
@@ -636,7 +662,7 @@ __global__ void __launch_bounds__(256) cast_flat_kernel(const uint16_t* __restri
         amax_pair = dev::absmax_pair(amax_pair, v[u].y);
         amax_pair = dev::absmax_pair(amax_pair, v[u].z);
         amax_pair = dev::absmax_pair(amax_pair, v[u].w);
-        if (ch < chunks) reinterpret_cast<uint2*>(q)[ch] = dev::cast8<FMT>(v[u], scale);
+        if (ch < chunks) store_q8<KEEP>(reinterpret_cast<uint2*>(q) + ch, dev::cast8<FMT>(v[u], scale));
     }
     if (blockIdx.x == 0 && tid == 0) {
         const int64_t t0 = chunks << 3;
@@ -783,14 +809,12 @@ cudaError_t launch_convert_f32(const float* in, int64_t n, int fmt, uint8_t* out
 
 cudaError_t launch_cast_flat(const uint16_t* x, int64_t n, uint8_t* q, const float* scale,
                              float* amax, float* scale_inv, int fmt, const float* noop,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, bool keep_q) {
     const int64_t chunks = n >> 3;
     const dim3 grid(grid_for((chunks + kFlatChunks - 1) / kFlatChunks, int64_t(1) << 30)), block(256);
-    if (fmt == 0)
-        return launch_pdl(cast_flat_kernel<0>, grid, block, 0, stream, x, n, q, scale, amax,
-                          scale_inv, noop);
-    return launch_pdl(cast_flat_kernel<1>, grid, block, 0, stream, x, n, q, scale, amax, scale_inv,
-                      noop);
+    auto k = fmt == 0 ? (keep_q ? cast_flat_kernel<0, true> : cast_flat_kernel<0, false>)
+                      : (keep_q ? cast_flat_kernel<1, true> : cast_flat_kernel<1, false>);
+    return launch_pdl(k, grid, block, 0, stream, x, n, q, scale, amax, scale_inv, noop);
 }
 
 constexpr int64_t kTransposeLoopPercent = 90;

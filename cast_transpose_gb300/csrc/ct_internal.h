@@ -143,10 +143,12 @@ cudaError_t launch_direct_list(const DirectParams<kMaxListPerLaunch>& p, int fmt
 // General path.
 cudaError_t launch_general(const GeneralArgs& a, int fmt, cudaStream_t stream);
 // q[i] = fp8(x[i] * scale) over n elements as one array (x 16-byte, q 8-byte
-// aligned), amax max-merged, scale_inv written.
+// aligned), amax max-merged, scale_inv written.  `keep_q`: q is stored with
+// the L2 evict-last priority, for a transpose that reads it next (which
+// lowers the priority again as it stages the lines).
 cudaError_t launch_cast_flat(const uint16_t* x, int64_t n, uint8_t* q, const float* scale,
                              float* amax, float* scale_inv, int fmt, const float* noop,
-                             cudaStream_t stream);
+                             cudaStream_t stream, bool keep_q = false);
 
 // Dbias schedule and partial sums.  The TMA kernel splits the R = ceil(rows
 // / 128) tile rows into bands of H = min(kDbiasBand, R) tile rows (the last
