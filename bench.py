@@ -783,12 +783,28 @@ def secondary(dev, peaks, args) -> dict:
         ms, best, 4 * x.numel() + 12, peaks, "direct_cast_transpose_kernel (odd-row stores)")
     del x, q, qt
     # ragged: odd rows and cols (the flat cast, then the FP8 transpose of q)
+    sets = [(workloads.normal_bf16(8191, 12287, 1.0, 17 + k, dev),) for k in range(3)]
+    sets = [(xk,) + ct.empty_outputs(xk) for (xk,) in sets]
+    turn = [0]
+
+    def rotating():
+        xk, qk, qtk = sets[turn[0] % 3]
+        turn[0] += 1
+        ct.fp8_cast_transpose(xk, s1, a0, si0, qk, qtk, ct.E4M3)
+
+    ms, best = _timed(torch, rotating, per_graph=12)
+    res["cast_transpose 8191x12287 E4M3 (ragged), three buffer sets"] = _rate_entry(
+        ms, best, 4 * sets[0][0].numel() + 12, peaks,
+        "as the next line, each call on the next of three (x, q, qT) sets: no line of q or qT "
+        "is reused from the call before")
+    del sets
     x = workloads.normal_bf16(8191, 12287, 1.0, 17, dev)
     q, qt = ct.empty_outputs(x)
     ms, best = _timed(torch, lambda: ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3))
     res["cast_transpose 8191x12287 E4M3 (ragged)"] = _rate_entry(
         ms, best, 4 * x.numel() + 12, peaks,
-        "cast_flat_kernel, then transpose_odd_kernel (q read back, mostly from L2)")
+        "cast_flat_kernel (q stored with the L2 evict-last priority), then "
+        "transpose_odd_loop_kernel (tiles from the last one back, q mostly from L2)")
     ms, best = _timed(torch, lambda: ct.fp8_transpose(q, qt))
     res["transpose 8191x12287 FP8 (ragged)"] = _rate_entry(ms, best, 2 * x.numel(), peaks,
                                                             "transpose_odd_kernel")

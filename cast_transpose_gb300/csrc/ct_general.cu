@@ -471,6 +471,22 @@ __device__ __forceinline__ void odd_transpose_tile(const uint8_t* __restrict__ i
             ibeg + uintptr_t(row0 - gen::kHaloRows + wr_hi - 1) * uintptr_t(cols) + uintptr_t(col0) +
             uintptr_t(ncol);
         const bool inside = (first & ~uintptr_t(15)) >= ibeg && ((last_end + 15) & ~uintptr_t(15)) <= iend;
+        if (inside && wr_lo == 0 && wr_hi == kOddStgRows && ncol == kTileCols) {
+            // A whole tile with its halo: all 144 rows, 128 bytes each (of
+            // chunk 8 only when the row does not start on a 16-byte boundary),
+            // unrolled, without the row range checks.
+#pragma unroll
+            for (int i = 0; i < 6; ++i) {
+                const int w = wr + 28 * i;
+                if (i == 5 && w >= kOddStgRows) break;
+                const uintptr_t ai = a + uintptr_t(i) * step;
+                if (k == 8 && (ai & 15) == 0) continue;
+                dev::cp_async16(stg + w * kOddStgPitch + 16 * k,
+                                reinterpret_cast<const void*>((ai & ~uintptr_t(15)) + 16 * uintptr_t(k)),
+                                16);
+            }
+            wr = kOddStgRows;
+        }
         for (; wr < kOddStgRows; wr += 28, a += step) {
             if (wr < wr_lo || wr >= wr_hi) continue;
             const int e = static_cast<int>(a & 15);
