@@ -812,7 +812,7 @@ def secondary(dev, peaks, args) -> dict:
     ms, best = _timed(torch, lambda: ct.fp8_transpose(q, qt, noop_flag=flag))
     res["transpose 8191x12287 FP8 (ragged), noop flag 0"] = _rate_entry(
         ms, best, 2 * x.numel(), peaks,
-        "transpose_odd_kernel: a looping first wave over 90% of the tiles, then one tile per CTA")
+        "transpose_odd_loop_kernel: a looping first wave over 90% of the tiles, then one tile per CTA")
     flag.fill_(1.0)
     ms, best = _timed(torch, lambda: ct.fp8_transpose(q, qt, noop_flag=flag), per_graph=50)
     res["transpose 8191x12287 FP8 (ragged), noop flag 1"] = {
