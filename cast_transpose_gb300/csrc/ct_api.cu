@@ -195,16 +195,20 @@ int cast_impl(const void* x, int64_t rows, int64_t cols, const float* scale, flo
     // faster (8192x12284: 5.01 against 4.29 TB/s).
     if (partial == nullptr && pend == nullptr && out != nullptr && aligned(x, 16) &&
         aligned(out, 8) && (out_t == nullptr || rows % 16 != 0)) {
-        const cudaError_t e = ct::launch_cast_flat(static_cast<const uint16_t*>(x), rows * cols,
-                                                   static_cast<uint8_t*>(out), scale, amax,
-                                                   scale_inv, fmt, noop, stream,
-                                                   /*keep_q=*/out_t != nullptr);
-        if (e != cudaSuccess || out_t == nullptr) return cuda_status(e);
+        // A transpose to follow over at least one wave of tiles: q is stored
+        // with the L2 evict-last priority and read back by the looping launch,
+        // which demotes its lines (ct::launch_transpose).
         const bool tfast = rows % 16 == 0 && cols % 16 == 0 && aligned(out, 16) &&
                            aligned(out_t, 16);
+        const bool keep =
+            out_t != nullptr && !tfast && ct::odd_transpose_loops_after_cast(rows, cols);
+        const cudaError_t e = ct::launch_cast_flat(static_cast<const uint16_t*>(x), rows * cols,
+                                                   static_cast<uint8_t*>(out), scale, amax,
+                                                   scale_inv, fmt, noop, stream, /*keep_q=*/keep);
+        if (e != cudaSuccess || out_t == nullptr) return cuda_status(e);
         return cuda_status(ct::launch_transpose(static_cast<const uint8_t*>(out), rows, cols,
                                                 static_cast<uint8_t*>(out_t), noop, tfast,
-                                                stream, /*after_cast=*/true));
+                                                stream, /*after_cast=*/keep));
     }
     ct::GeneralArgs a;
     a.x = static_cast<const uint16_t*>(x);

@@ -872,6 +872,12 @@ int odd_transpose_wave_ctas() {
     return cache[dev];
 }
 
+bool odd_transpose_loops_after_cast(int64_t rows, int64_t cols) {
+    const int64_t tiles = ((rows + 127) / 128) * ((cols + 127) / 128);
+    const int wave = odd_transpose_wave_ctas();
+    return wave > 0 && tiles >= wave;
+}
+
 cudaError_t launch_transpose(const uint8_t* in, int64_t rows, int64_t cols, uint8_t* out,
                              const float* noop, bool fast, cudaStream_t stream, bool after_cast) {
     if (fast) {

@@ -192,11 +192,16 @@ cudaError_t launch_scale_update_pending(float* hist, float* pending, float* scal
                                         const float* noop, cudaStream_t stream);
 
 // FP8 byte transpose.  `fast` requires rows % 16 == 0, cols % 16 == 0 and
-// 16-byte aligned pointers.  `after_cast`: the transpose of a q that the flat
-// cast has just written (the odd-shape kernel then takes the looping launch).
+// 16-byte aligned pointers.  `after_cast` (odd shapes, only where
+// odd_transpose_loops_after_cast holds): the transpose of a q that the flat
+// cast has just stored with the L2 evict-last priority; the looping launch
+// then takes the tiles in reverse order and demotes the lines it stages.
 cudaError_t launch_transpose(const uint8_t* in, int64_t rows, int64_t cols, uint8_t* out,
                              const float* noop, bool fast, cudaStream_t stream,
                              bool after_cast = false);
+// Whether a rows x cols odd-shape transpose has at least one wave of tiles
+// for the looping launch (smaller ones keep one tile per CTA after the cast).
+bool odd_transpose_loops_after_cast(int64_t rows, int64_t cols);
 
 // FP8 conversion of n fp32 values (no scale): the cast kernels' conversion step.
 cudaError_t launch_convert_f32(const float* in, int64_t n, int fmt, uint8_t* out,

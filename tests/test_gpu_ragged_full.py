@@ -97,3 +97,27 @@ def test_ragged_kernel_row_ends(shape, x_shift, out_off):
     assert np.array_equal(qt.numpy().reshape(cols, rows), ref["qt"])
     assert f32_bits(a.item()) == f32_bits(ref["amax"])
     assert f32_bits(si.item()) == f32_bits(ref["scale_inv"])
+
+
+@pytest.mark.parametrize("flag", [None, 0.0])
+@pytest.mark.parametrize("shape", [(2000, 5003), (1937, 9731)])
+def test_flat_cast_then_transpose_from_one_wave(shape, flag):
+    """Shapes of 640 and 1232 tiles: the flat cast stores q with the L2
+    evict-last priority and the looping transpose launch takes the tiles from
+    the last one back, demoting the lines it stages; with no noop flag and
+    with one at 0.  Every byte of q and qT against the oracle."""
+    rows, cols = shape
+    x_cpu = workloads.normal_bf16(rows, cols, 4.0, rows + cols)
+    n = rows * cols
+    q, qt = Guarded(n), Guarded(n)
+    s, a, si = scalar(0.8125), scalar(0.0), scalar(-1.0)
+    noop = None if flag is None else torch.full((1,), flag, device="cuda")
+    ct.fp8_cast_transpose(x_cpu.cuda(), s, a, si, q.t, qt.t, ct.E4M3, noop_flag=noop)
+    torch.cuda.synchronize()
+    q.check()
+    qt.check()
+    ref = oracle.cast_transpose(x_cpu, 0.8125, ct.E4M3)
+    assert np.array_equal(q.numpy().reshape(rows, cols), ref["q"])
+    assert np.array_equal(qt.numpy().reshape(cols, rows), ref["qt"])
+    assert f32_bits(a.item()) == f32_bits(ref["amax"])
+    assert f32_bits(si.item()) == f32_bits(ref["scale_inv"])
