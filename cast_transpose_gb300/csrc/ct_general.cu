@@ -439,11 +439,10 @@ constexpr int kOddStgRows = gen::kHaloRows + kTileRows;   // 144 staged rows
 constexpr int kOddStgPitch = 144;                         // 9 chunks of 16 bytes
 
 // One tile of the odd-shape transpose (the staging, gather and stores above).
-__device__ __forceinline__ void odd_transpose_tile(const uint8_t* __restrict__ in, int64_t rows,
-                                                   int64_t cols, uint8_t* __restrict__ out,
-                                                   uint32_t t, uint32_t tiles_c, uint8_t* stg,
-                                                   uint8_t* sqt, int tid, int lane, int warp,
-                                                   bool demote = false) {
+// Copies of tile t's 144 staged rows into stg (cp.async, not waited for).
+__device__ __forceinline__ void odd_stage_tile(const uint8_t* __restrict__ in, int64_t rows,
+                                               int64_t cols, uint32_t t, uint32_t tiles_c,
+                                               uint8_t* stg, int tid) {
     const uint32_t rt32 = t / tiles_c;
     const int64_t rt = rt32;
     const int64_t row0 = rt * kTileRows;
@@ -504,6 +503,26 @@ __device__ __forceinline__ void odd_transpose_tile(const uint8_t* __restrict__ i
             }
         }
     }
+}
+
+// Tile t: its staged rows (copied here unless `staged`), the gather into the
+// column-major copy, and the whole-block stores.  `next` >= 0: the copies of
+// tile `next` are issued into stg once the gather is done, so that they land
+// while this tile's stores run.
+__device__ __forceinline__ void odd_transpose_tile(const uint8_t* __restrict__ in, int64_t rows,
+                                                   int64_t cols, uint8_t* __restrict__ out,
+                                                   uint32_t t, uint32_t tiles_c, uint8_t* stg,
+                                                   uint8_t* sqt, int tid, int lane, int warp,
+                                                   bool demote = false, bool staged = false,
+                                                   int64_t next = -1) {
+    const uint32_t rt32 = t / tiles_c;
+    const int64_t rt = rt32;
+    const int64_t row0 = rt * kTileRows;
+    const int64_t col0 = int64_t(t - rt32 * tiles_c) * kTileCols;
+    const int ncol = static_cast<int>(cols - col0 < kTileCols ? cols - col0 : kTileCols);
+    const uintptr_t ibeg = reinterpret_cast<uintptr_t>(in);
+
+    if (!staged) odd_stage_tile(in, rows, cols, t, tiles_c, stg, tid);
     dev::cp_async_wait_all();
     __syncthreads();
     if (demote) {   // the tile's own q rows, now staged, back to the normal L2 priority
@@ -568,7 +587,8 @@ __device__ __forceinline__ void odd_transpose_tile(const uint8_t* __restrict__ i
         for (int kq = 0; kq < 4; ++kq)
             *reinterpret_cast<uint32_t*>(col + ((kq + rot) & 3) * gen::kColCopyPitch) = c[kq];
     }
-    __syncthreads();
+    __syncthreads();   // the gather is done with stg
+    if (next >= 0) odd_stage_tile(in, rows, cols, static_cast<uint32_t>(next), tiles_c, stg, tid);
     gen::store_col_copy_blocks(out, rows, cols, rt, row0, col0, sqt, lane, warp);
 }
 
@@ -615,12 +635,18 @@ __global__ void __launch_bounds__(256, 4) transpose_odd_loop_kernel(const uint8_
     } else {
         first = uint32_t(loop_ctas) * uint32_t(loop_tiles) + (blockIdx.x - loop_ctas);
     }
-    // A tile's gather ends before the barrier in front of its stores, so the
-    // next tile's staging never overwrites rows still being read.
+    // A tile's gather ends at the barrier in front of its stores; the copies
+    // of the CTA's next tile are issued there, into the staging rows the
+    // gather has finished with, and land while the stores run.
     uint32_t t = first;
-    for (uint32_t kt = 0; kt < count && t < tiles; ++kt, t += stride)
+    if (count > 0 && t < tiles)
+        odd_stage_tile(in, rows, cols, reverse ? tiles - 1 - t : t, tiles_c, stg, tid);
+    for (uint32_t kt = 0; kt < count && t < tiles; ++kt, t += stride) {
+        const uint32_t tn = t + stride;
+        const int64_t next = kt + 1 < count && tn < tiles ? int64_t(reverse ? tiles - 1 - tn : tn) : -1;
         odd_transpose_tile(in, rows, cols, out, reverse ? tiles - 1 - t : t, tiles_c, stg, sqt, tid,
-                           lane, warp, reverse != 0);
+                           lane, warp, reverse != 0, /*staged=*/true, next);
+    }
 }
 
 
