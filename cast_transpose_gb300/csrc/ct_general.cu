@@ -417,7 +417,8 @@ __global__ void __launch_bounds__(256) transpose_fast_kernel(const uint8_t* __re
 // registers, else byte loads (first and last blocks of `in` only); bytes past
 // the row end are zeroed.  The transposed 16-byte blocks are stored with
 // gen::store_segment_x8 (aligned 16-byte blocks, masked at the segment ends).
-// FP8 transpose of any shape and alignment, one 128x128 tile per CTA.
+// FP8 transpose of any shape and alignment, in 128x128 tiles (one per CTA,
+// or a looping first wave: see transpose_odd_loop_kernel).
 //   * Staging: row r of the tile is the byte segment in + g * cols + col0 of
 //     ncol bytes, starting e_r = its address % 16 into a 16-byte chunk.  The
 //     nine aligned chunks that cover it are copied as they are (cp.async, 16
@@ -432,13 +433,14 @@ __global__ void __launch_bounds__(256) transpose_fast_kernel(const uint8_t* __re
 //     e_r is the same for the whole warp.  Since e_{r+1} = e_r + cols (mod
 //     16), e_r depends on the row within the 16-row block only.  Byte
 //     permutes transpose each 4x4 block; the column pieces go to a
-//     column-major copy.  Warps 0 .. 3 also take 4 halo rows each (warp 0
-//     taking all 16 left the other seven waiting for it at the barrier).
+//     column-major copy, each lane's four columns in a rotated order that
+//     keeps the copy's stores free of bank conflicts.  Warps 0 .. 3 also
+//     take 4 halo rows each (warp 0 taking all 16 left the other seven
+//     waiting for it at the barrier).
 //   * Stores: gen::store_col_copy_blocks, whole aligned 16-byte blocks.
 constexpr int kOddStgRows = gen::kHaloRows + kTileRows;   // 144 staged rows
 constexpr int kOddStgPitch = 144;                         // 9 chunks of 16 bytes
 
-// One tile of the odd-shape transpose (the staging, gather and stores above).
 // Copies of tile t's 144 staged rows into stg (cp.async, not waited for).
 __device__ __forceinline__ void odd_stage_tile(const uint8_t* __restrict__ in, int64_t rows,
                                                int64_t cols, uint32_t t, uint32_t tiles_c,
