@@ -8,6 +8,11 @@ spawned oracle processes on all host cores).
     aligned qT blocks with a halo from the tile above);
   * 8191 x 12287 FP8 transpose of an existing q, and of a q that starts at an
     odd byte, written to a qT at an odd byte.
+
+Smaller cases (against the single-process oracle) cover row ends off the
+direct kernel's alignment, and the flat cast + transpose from one wave of
+tiles of the looping launch (q stored evict-last, tiles in reverse order),
+with and without a noop flag at 0.
 """
 import numpy as np
 import pytest
