@@ -193,8 +193,8 @@ int cast_impl(const void* x, int64_t rows, int64_t cols, const float* scale, flo
     // (8191x12287: 4.5 TB/s against 3.49 for the general kernel); with rows %
     // 16 == 0 the general kernel's transposed stores are aligned, and it stays
     // faster (8192x12284: 5.01 against 4.29 TB/s).
-    if (partial == nullptr && pend == nullptr && out != nullptr && aligned(x, 16) &&
-        aligned(out, 8) && (out_t == nullptr || rows % 16 != 0)) {
+    if (partial == nullptr && pend == nullptr && out != nullptr && aligned(out, 8) &&
+        (out_t == nullptr || rows % 16 != 0)) {
         // A transpose to follow over at least one wave of tiles: q is stored
         // with the L2 evict-last priority and read back by the looping launch,
         // which demotes its lines (ct::launch_transpose).

@@ -738,6 +738,125 @@ __global__ void __launch_bounds__(256) cast_flat_kernel(const uint16_t* __restri
     }
 }
 
+// The flat cast of an x that starts m bytes past a 16-byte boundary (m = 2,
+// 4, .., 14, the same for every element): output chunk c, x[8c .. 8c + 7],
+// is bytes m .. m + 15 of the aligned chunks c and c + 1 of xa = x - m bytes.
+// A warp loads 32 consecutive aligned chunks G .. G + 31 and writes the 31
+// output chunks G .. G + 30, lane l taking chunk G + l + 1 from lane l + 1 by
+// a shuffle (so every 32nd aligned chunk is loaded twice, and no lane waits
+// on a load of its own after the first).  Group g of a CTA's 64 groups (8
+// warps x kFlatPerThread) starts at G = 31 (64 blockIdx + 8 u + warp).
+// Aligned chunk `chunks` (n / 8), the one that can reach past the end of x,
+// is put together from x's elements, so no byte outside x is read except the
+// m bytes before x in aligned chunk 0 (inside x's allocation, whose start is
+// 16-byte aligned).
+constexpr int64_t kShiftGroups = 8 * kFlatPerThread;   // 31-chunk groups per CTA
+
+__device__ __forceinline__ uint4 flat_tail_chunk(const uint16_t* __restrict__ x, int64_t n,
+                                                 int64_t first) {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int64_t i = first + 2 * k;
+        const uint32_t lo = i >= 0 && i < n ? x[i] : 0u;
+        const uint32_t hi = i + 1 >= 0 && i + 1 < n ? x[i + 1] : 0u;
+        w[k] = lo | (hi << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Bytes m .. m + 15 of the 32-byte window (a, b), m = 4 * WD + 2 * H.
+template <int WD>
+__device__ __forceinline__ uint4 window16(const uint4& a, const uint4& b, int sh) {
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    return make_uint4(__funnelshift_r(w[WD], w[WD + 1], sh), __funnelshift_r(w[WD + 1], w[WD + 2], sh),
+                      __funnelshift_r(w[WD + 2], w[WD + 3], sh), __funnelshift_r(w[WD + 3], w[WD + 4], sh));
+}
+
+template <int FMT, bool KEEP, int WD>
+__device__ __forceinline__ void flat_shift_body(const uint16_t* __restrict__ x, int64_t n,
+                                                uint8_t* __restrict__ q, float scale, int m,
+                                                uint32_t& amax_pair) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint4* xa = reinterpret_cast<const uint4*>(reinterpret_cast<uintptr_t>(x) - m);
+    const int64_t chunks = n >> 3;
+    const int64_t g0 = int64_t(blockIdx.x) * kShiftGroups + warp;
+    const int sh = 8 * (m & 3);
+    uint4 a[kFlatPerThread];
+#pragma unroll
+    for (int u = 0; u < kFlatPerThread; ++u) {
+        const int64_t j = 31 * (g0 + 8 * u) + lane;   // aligned chunk of this lane
+        a[u] = j < chunks ? __ldcs(xa + j)
+                          : (j == chunks ? flat_tail_chunk(x, n, 8 * j - m / 2) : make_uint4(0u, 0u, 0u, 0u));
+    }
+#pragma unroll
+    for (int u = 0; u < kFlatPerThread; ++u) {
+        const int64_t ch = 31 * (g0 + 8 * u) + lane;   // output chunk of this lane (lanes 0 .. 30)
+        uint4 b;
+        b.x = __shfl_down_sync(0xFFFFFFFFu, a[u].x, 1);
+        b.y = __shfl_down_sync(0xFFFFFFFFu, a[u].y, 1);
+        b.z = __shfl_down_sync(0xFFFFFFFFu, a[u].z, 1);
+        b.w = __shfl_down_sync(0xFFFFFFFFu, a[u].w, 1);
+        if (lane < 31 && ch < chunks) {
+            const uint4 v = window16<WD>(a[u], b, sh);
+            amax_pair = dev::absmax_pair(amax_pair, v.x);
+            amax_pair = dev::absmax_pair(amax_pair, v.y);
+            amax_pair = dev::absmax_pair(amax_pair, v.z);
+            amax_pair = dev::absmax_pair(amax_pair, v.w);
+            store_q8<KEEP>(reinterpret_cast<uint2*>(q) + ch, dev::cast8<FMT>(v, scale));
+        }
+    }
+}
+
+template <int FMT, bool KEEP>
+__global__ void __launch_bounds__(256) cast_flat_shift_kernel(const uint16_t* __restrict__ x,
+                                                              int64_t n, uint8_t* __restrict__ q,
+                                                              const float* scale_p, float* amax,
+                                                              float* scale_inv, const float* noop) {
+    dev::pdl_launch_dependents();
+    dev::pdl_wait();
+    if (noop != nullptr && *noop != 0.0f) return;
+    __shared__ unsigned s_amax[8];
+    const float scale = *scale_p;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int m = static_cast<int>(reinterpret_cast<uintptr_t>(x) & 15);
+    uint32_t amax_pair = 0;
+    switch (m >> 2) {   // the same for the whole grid
+        case 0: flat_shift_body<FMT, KEEP, 0>(x, n, q, scale, m, amax_pair); break;
+        case 1: flat_shift_body<FMT, KEEP, 1>(x, n, q, scale, m, amax_pair); break;
+        case 2: flat_shift_body<FMT, KEEP, 2>(x, n, q, scale, m, amax_pair); break;
+        default: flat_shift_body<FMT, KEEP, 3>(x, n, q, scale, m, amax_pair); break;
+    }
+    if (blockIdx.x == 0 && tid == 0) {
+        const int64_t t0 = (n >> 3) << 3;
+        if (t0 < n) {   // the last n % 8 elements
+            uint32_t e[4] = {0u, 0u, 0u, 0u};
+            for (int64_t i = t0; i < n; ++i)
+                e[(i - t0) >> 1] |= uint32_t(x[i]) << (16 * ((i - t0) & 1));
+            const uint4 t = make_uint4(e[0], e[1], e[2], e[3]);
+            amax_pair = dev::absmax_pair(amax_pair, t.x);
+            amax_pair = dev::absmax_pair(amax_pair, t.y);
+            amax_pair = dev::absmax_pair(amax_pair, t.z);
+            amax_pair = dev::absmax_pair(amax_pair, t.w);
+            const uint2 c = dev::cast8<FMT>(t, scale);
+            for (int64_t i = t0; i < n; ++i) {
+                const int k = static_cast<int>(i - t0);
+                q[i] = static_cast<uint8_t>((k < 4 ? c.x : c.y) >> (8 * (k & 3)));
+            }
+        }
+        *scale_inv = __fdiv_rn(1.0f, scale);
+    }
+    const unsigned mx = __reduce_max_sync(0xFFFFFFFFu, dev::pair_to_f32_bits(amax_pair));
+    if (lane == 0) s_amax[warp] = mx;
+    __syncthreads();
+    if (tid == 0) {
+        unsigned a = s_amax[0];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) a = a > s_amax[w] ? a : s_amax[w];
+        if (a != 0) atomicMax(reinterpret_cast<unsigned*>(amax), a);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // The conversion step alone: out[i] = fp8(in[i]) through dev::cvt_fp8x2, the
 // routine every cast kernel applies to x * scale.  Grid-stride over pairs of
@@ -856,6 +975,13 @@ cudaError_t launch_cast_flat(const uint16_t* x, int64_t n, uint8_t* q, const flo
                              cudaStream_t stream, bool keep_q) {
     const int64_t chunks = n >> 3;
     const dim3 grid(grid_for((chunks + kFlatChunks - 1) / kFlatChunks, int64_t(1) << 30)), block(256);
+    if (reinterpret_cast<uintptr_t>(x) & 15) {
+        const int64_t groups = (chunks + 30) / 31;
+        const dim3 sgrid(grid_for((groups + kShiftGroups - 1) / kShiftGroups, int64_t(1) << 30));
+        auto k = fmt == 0 ? (keep_q ? cast_flat_shift_kernel<0, true> : cast_flat_shift_kernel<0, false>)
+                          : (keep_q ? cast_flat_shift_kernel<1, true> : cast_flat_shift_kernel<1, false>);
+        return launch_pdl(k, sgrid, block, 0, stream, x, n, q, scale, amax, scale_inv, noop);
+    }
     auto k = fmt == 0 ? (keep_q ? cast_flat_kernel<0, true> : cast_flat_kernel<0, false>)
                       : (keep_q ? cast_flat_kernel<1, true> : cast_flat_kernel<1, false>);
     return launch_pdl(k, grid, block, 0, stream, x, n, q, scale, amax, scale_inv, noop);
