@@ -798,6 +798,16 @@ def secondary(dev, peaks, args) -> dict:
         "as the next line, each call on the next of three (x, q, qT) sets: no line of q or qT "
         "is reused from the call before")
     del sets
+    xbuf = torch.empty(8191 * 12287 + 8, dtype=torch.bfloat16, device=dev)
+    x = xbuf[1:1 + 8191 * 12287].view(8191, 12287)
+    x.copy_(workloads.normal_bf16(8191, 12287, 1.0, 17, dev))
+    q, qt = ct.empty_outputs(x)
+    ms, best = _timed(torch, lambda: ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3))
+    res["cast_transpose 8191x12287 E4M3 (ragged, x 2 bytes past a 16-byte boundary)"] = _rate_entry(
+        ms, best, 4 * x.numel() + 12, peaks,
+        "cast_flat_shift_kernel (aligned chunks shifted by x's offset), then "
+        "transpose_odd_loop_kernel")
+    del xbuf, x, q, qt
     x = workloads.normal_bf16(8191, 12287, 1.0, 17, dev)
     q, qt = ct.empty_outputs(x)
     ms, best = _timed(torch, lambda: ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3))
@@ -1066,8 +1076,10 @@ def profile_case(name: str) -> None:
                     three 48-column scale updates;
       'cast':       cast only of the activation, then three FP8 transposes;
       'general':    cast-transpose of a ragged 8191x12287 matrix whose x
-                    starts 2 bytes past a 16-byte boundary (the general cast
-                    kernel);
+                    starts 2 bytes past a 16-byte boundary and whose q and qT
+                    start 1 byte past one (the general cast kernel);
+      'shifted':    the same x with aligned q and qT (the flat cast of a
+                    shifted x, then the odd-shape transpose);
       'ragged':     cast-transpose of a ragged 8191x12287 matrix (the flat cast
                     kernel, then the FP8 transpose of q), then three FP8
                     transposes of q (the odd-shape transpose kernel);
@@ -1113,6 +1125,15 @@ def profile_case(name: str) -> None:
         for _ in range(3):
             ct.fp8_transpose(q, qt)
     elif name == "general":
+        n = 8191 * 12287
+        buf = torch.empty(n + 8, dtype=torch.bfloat16, device=dev)
+        x = buf[1:1 + n].view(8191, 12287)
+        x.copy_(workloads.normal_bf16(8191, 12287, 1.0, 17, dev))
+        qbuf = torch.empty(2 * n + 32, dtype=torch.uint8, device=dev)
+        q, qt = qbuf[1:1 + n].view(8191, 12287), qbuf[n + 17:2 * n + 17].view(12287, 8191)
+        for _ in range(3):
+            ct.fp8_cast_transpose(x, s1, a0, si0, q, qt, ct.E4M3)
+    elif name == "shifted":
         buf = torch.empty(8191 * 12287 + 8, dtype=torch.bfloat16, device=dev)
         x = buf[1:1 + 8191 * 12287].view(8191, 12287)
         x.copy_(workloads.normal_bf16(8191, 12287, 1.0, 17, dev))
@@ -1179,8 +1200,8 @@ def _parse(argv=None):
     ap.add_argument("--extra", action=argparse.BooleanOptionalAction, default=True,
                     help="also time the secondary workloads")
     ap.add_argument("--profile-case",
-                    choices=["activation", "gradient", "list", "cast", "general", "ragged", "flat",
-                             "odd",
+                    choices=["activation", "gradient", "list", "cast", "general", "shifted", "ragged",
+                             "flat", "odd",
                              "loop", "noop", "weight"],
                     default=None,
                     help="only run 3 launches of one workload's kernel (for ncu) and exit")

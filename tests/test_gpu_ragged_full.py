@@ -6,9 +6,9 @@ spawned oracle processes on all host cores).
     transpose of q;
   * 8191 x 12288 cast-transpose: the direct kernel's odd-row variant (whole
     aligned qT blocks with a halo from the tile above);
-  * 8191 x 12287 and 8192 x 12288 cast-transposes of an x 2 and 14 bytes
+  * 8191 x 12287 and 8191 x 12288 cast-transposes of an x 2 and 14 bytes
     past a 16-byte boundary: the flat cast of a shifted x, then the odd-shape
-    or the aligned transpose;
+    transpose;
   * 8191 x 12287 FP8 transpose of an existing q, and of a q that starts at an
     odd byte, written to a qT at an odd byte.
 
@@ -40,7 +40,7 @@ def _no_device_error():
 @pytest.mark.parametrize("shape,fmt,x_shift", [((8191, 12287), ct.E4M3, 0),
                                                ((8191, 12288), ct.E5M2, 0),
                                                ((8191, 12287), ct.E4M3, 1),
-                                               ((8192, 12288), ct.E5M2, 7)])
+                                               ((8191, 12288), ct.E5M2, 7)])
 def test_ragged_cast_transpose_in_full(shape, fmt, x_shift):
     """x_shift: x starts that many bf16 elements past a 16-byte boundary (the
     flat cast then shifts every chunk by the same byte offset)."""
