@@ -53,10 +53,12 @@
  *     buffers, take a fast path: a persistent TMA-staged kernel for launches
  *     under 2048 tiles of 128x128, a direct-load kernel (256 threads per
  *     tile) from 2048 tiles on.  Other row counts with cols a multiple of 8
- *     and aligned buffers take the direct-load kernel.  A plain cast
- *     (ct_fp8_cast) of any other shape with x 16-byte and out 8-byte aligned
- *     runs over the rows * cols elements as one flat array.  Everything else
- *     takes a slower general kernel.  All give identical results.
+ *     and aligned buffers take the direct-load kernel.  With out 8-byte
+ *     aligned and no dbias, a plain cast (ct_fp8_cast) of any other shape or
+ *     x alignment runs over the rows * cols elements as one flat array, and
+ *     so does a cast-transpose with rows not a multiple of 16, followed by an
+ *     FP8 transpose of out into out_t.  Everything else takes a slower
+ *     general kernel.  All give identical results.
  *   - Calls are thread-safe; the library keeps no per-call state.  The first
  *     call of an entry point on a device also sets its kernels' shared-memory
  *     limit (cudaFuncSetAttribute, once per device): make that first call
