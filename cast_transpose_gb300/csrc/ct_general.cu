@@ -744,13 +744,17 @@ __global__ void __launch_bounds__(256) cast_flat_kernel(const uint16_t* __restri
 // A warp loads 32 consecutive aligned chunks G .. G + 31 and writes the 31
 // output chunks G .. G + 30, lane l taking chunk G + l + 1 from lane l + 1 by
 // a shuffle (so every 32nd aligned chunk is loaded twice, and no lane waits
-// on a load of its own after the first).  Group g of a CTA's 64 groups (8
-// warps x kFlatPerThread) starts at G = 31 (64 blockIdx + 8 u + warp).
+// on a load of its own after the first).  Group g of a CTA's 48 groups (8
+// warps x kShiftPerThread) starts at G = 31 (48 blockIdx + 8 u + warp).
+// Six loads in flight per thread keep it within 48 registers: 5 CTAs per
+// SM (8191x12287 cast only, against eight loads at 4 CTAs per SM: 6.67
+// against 6.58 TB/s).
 // Aligned chunk `chunks` (n / 8), the one that can reach past the end of x,
 // is put together from x's elements, so no byte outside x is read except the
 // m bytes before x in aligned chunk 0 (inside x's allocation, whose start is
 // 16-byte aligned).
-constexpr int64_t kShiftGroups = 8 * kFlatPerThread;   // 31-chunk groups per CTA
+constexpr int kShiftPerThread = 6;
+constexpr int64_t kShiftGroups = 8 * kShiftPerThread;   // 31-chunk groups per CTA
 
 __device__ __forceinline__ uint4 flat_tail_chunk(const uint16_t* __restrict__ x, int64_t n,
                                                  int64_t first) {
@@ -782,15 +786,15 @@ __device__ __forceinline__ void flat_shift_body(const uint16_t* __restrict__ x, 
     const int64_t chunks = n >> 3;
     const int64_t g0 = int64_t(blockIdx.x) * kShiftGroups + warp;
     const int sh = 8 * (m & 3);
-    uint4 a[kFlatPerThread];
+    uint4 a[kShiftPerThread];
 #pragma unroll
-    for (int u = 0; u < kFlatPerThread; ++u) {
+    for (int u = 0; u < kShiftPerThread; ++u) {
         const int64_t j = 31 * (g0 + 8 * u) + lane;   // aligned chunk of this lane
         a[u] = j < chunks ? __ldcs(xa + j)
                           : (j == chunks ? flat_tail_chunk(x, n, 8 * j - m / 2) : make_uint4(0u, 0u, 0u, 0u));
     }
 #pragma unroll
-    for (int u = 0; u < kFlatPerThread; ++u) {
+    for (int u = 0; u < kShiftPerThread; ++u) {
         const int64_t ch = 31 * (g0 + 8 * u) + lane;   // output chunk of this lane (lanes 0 .. 30)
         uint4 b;
         b.x = __shfl_down_sync(0xFFFFFFFFu, a[u].x, 1);
@@ -809,7 +813,7 @@ __device__ __forceinline__ void flat_shift_body(const uint16_t* __restrict__ x, 
 }
 
 template <int FMT, bool KEEP>
-__global__ void __launch_bounds__(256) cast_flat_shift_kernel(const uint16_t* __restrict__ x,
+__global__ void __launch_bounds__(256, 5) cast_flat_shift_kernel(const uint16_t* __restrict__ x,
                                                               int64_t n, uint8_t* __restrict__ q,
                                                               const float* scale_p, float* amax,
                                                               float* scale_inv, const float* noop) {
