@@ -6,7 +6,10 @@ aligned, runs as one flat array of rows * cols elements: 8-element chunks,
 then the last n % 8 elements by one thread.  The cases cover every tail
 length, the two ends of tiny arrays, q at an 8-byte but not 16-byte offset,
 NaN and Inf in the tail (amax propagation), the noop flag, and the 8191 x
-12287 matrix in full through the oracle on all host cores.
+12287 matrix in full through the oracle on all host cores.  An x that is not
+16-byte aligned takes the shifted flat cast: every even byte offset with
+every tail length, lengths around its 31-chunk warp groups, special values
+in the chunk assembled past the end of x, and the noop flag.
 """
 import numpy as np
 import pytest
@@ -104,3 +107,50 @@ def test_ragged_8191x12287_in_full():
     assert res["bad_q"] == 0, ("FP8 data differs from the oracle", res["first_q"])
     assert f32_bits(amax) == f32_bits(res["amax"])
     assert f32_bits(sinv) == f32_bits(np.float32(1.0))
+
+
+def _shifted(x_cpu, elems):
+    """x on the GPU `elems` bf16 elements past a 256-byte-aligned allocation."""
+    n = x_cpu.numel()
+    big = torch.empty(n + 16, dtype=torch.bfloat16, device="cuda")
+    big[elems:elems + n] = x_cpu.reshape(-1).cuda()
+    return big[elems:elems + n].view(x_cpu.shape)
+
+
+@pytest.mark.parametrize("x_shift", range(1, 8))
+@pytest.mark.parametrize("shape", TAILS + [(31, 8), (33, 8), (1, 248), (7, 1001), (300, 263)])
+def test_shifted_x_every_offset_and_tail(shape, x_shift):
+    """x 2, 4, .., 14 bytes past a 16-byte boundary (the shifted flat cast):
+    every tail length, arrays shorter than one chunk, lengths around a
+    31-chunk warp group, with q 8-byte aligned."""
+    x_cpu = workloads.normal_bf16(*shape, 40.0, 900 + 16 * x_shift + shape[0] * 7 + shape[1])
+    got = _cast(_shifted(x_cpu, x_shift), 0.375, ct.E4M3, q_offset=8 * (x_shift & 1))
+    _assert_oracle(x_cpu, 0.375, ct.E4M3, got)
+
+
+@pytest.mark.parametrize("x_shift", [1, 6])
+def test_shifted_x_nan_and_inf_near_the_end(x_shift):
+    """Special values in the last whole chunk and in the tail, reached
+    through the assembled chunk past the end of x."""
+    rows, cols = 37, 41
+    x_cpu = workloads.normal_bf16(rows, cols, 1.0, 77 + x_shift)
+    flat = x_cpu.reshape(-1)
+    n = flat.numel()
+    flat[n - 3] = float("inf")
+    flat[(n // 8) * 8 - 2] = float("-inf")
+    got = _cast(_shifted(x_cpu, x_shift), 1.0, ct.E5M2)
+    _assert_oracle(x_cpu, 1.0, ct.E5M2, got)
+    flat[n - 1] = float("nan")
+    got = _cast(_shifted(x_cpu, x_shift), 1.0, ct.E5M2)
+    _assert_oracle(x_cpu, 1.0, ct.E5M2, got)
+
+
+def test_shifted_x_noop_flag_set_writes_nothing():
+    x_cpu = workloads.normal_bf16(300, 263, 1.0, 5)
+    q = Guarded(300 * 263)
+    q.t.fill_(0x5A)
+    s, a, si = scalar(1.0), scalar(0.0), scalar(-1.0)
+    ct.fp8_cast(_shifted(x_cpu, 3), s, a, si, q.t, ct.E4M3, noop_flag=torch.ones(1, device="cuda"))
+    torch.cuda.synchronize()
+    q.check()
+    assert (q.numpy() == 0x5A).all() and a.item() == 0.0 and si.item() == -1.0
