@@ -1,10 +1,12 @@
 // ct_api.cu -- the C ABI of include/cast_transpose.h: host-side argument
 // checks, TMA descriptor encoding and dispatch between the persistent
 // TMA-staged kernel (fast shapes, under kDirectMinTiles tiles), the
-// direct-load kernel (fast shapes, from kDirectMinTiles tiles on) and the
-// general kernel (every other shape and alignment).  No device memory is allocated here, no stream or
-// device is synchronised, and no device memory is read, so every call can be
-// captured in a CUDA graph.
+// direct-load kernel (fast shapes, from kDirectMinTiles tiles on, and odd
+// row counts), the flat cast with the FP8 transpose of q (other shapes and
+// x alignments with q 8-byte aligned), and the general kernel (everything
+// else).  No device memory is allocated here, no stream or device is
+// synchronised, and no device memory is read, so every call can be captured
+// in a CUDA graph.
 #include "../../include/cast_transpose.h"
 #include "ct_internal.h"
 
@@ -187,12 +189,14 @@ int cast_impl(const void* x, int64_t rows, int64_t cols, const float* scale, flo
         if (runs_out) *runs_out = ct::dbias_units(R, R < ct::kDbiasBand ? R : ct::kDbiasBand).bands;
         return cuda_status(ct::launch_fast(p, fmt, partial != nullptr, out_t ? 0 : 1, stream));
     }
-    // With x 16-byte and q 8-byte aligned, q is one flat array of rows * cols
-    // elements whatever the row length: the flat cast writes it.  With a
-    // transpose and rows % 16 != 0, the FP8 transpose of q then writes qT
-    // (8191x12287: 4.5 TB/s against 3.49 for the general kernel); with rows %
+    // With q 8-byte aligned, q is one flat array of rows * cols elements
+    // whatever the row length: the flat cast writes it (an x off a 16-byte
+    // boundary through the shifted variant).  With a transpose and rows % 16
+    // != 0, the FP8 transpose of q then writes qT (8191x12287: 4.77 TB/s, x 2
+    // bytes off 4.62, against 3.49 / 3.45 for the general kernel); with rows %
     // 16 == 0 the general kernel's transposed stores are aligned, and it stays
-    // faster (8192x12284: 5.01 against 4.29 TB/s).
+    // faster (8192x12284: 5.01 against 4.29 TB/s; x 2 bytes off 5.15 against
+    // 4.30).
     if (partial == nullptr && pend == nullptr && out != nullptr && aligned(out, 8) &&
         (out_t == nullptr || rows % 16 != 0)) {
         // A transpose to follow over at least one wave of tiles: q is stored
