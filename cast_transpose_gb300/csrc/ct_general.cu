@@ -411,12 +411,6 @@ __global__ void __launch_bounds__(256) transpose_fast_kernel(const uint8_t* __re
     }
 }
 
-// General byte transpose: any shape, in and out at any byte.  128x128
-// tiles with the fast kernel's layout; each 16-byte row chunk is one aligned
-// load, else the two aligned blocks covering it (both inside `in`) shifted in
-// registers, else byte loads (first and last blocks of `in` only); bytes past
-// the row end are zeroed.  The transposed 16-byte blocks are stored with
-// gen::store_segment_x8 (aligned 16-byte blocks, masked at the segment ends).
 // FP8 transpose of any shape and alignment, in 128x128 tiles (one per CTA,
 // or a looping first wave: see transpose_odd_loop_kernel).
 //   * Staging: row r of the tile is the byte segment in + g * cols + col0 of
